@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of one LAMB optimizer step on one ZeRO-2 shard.
+
+Default workload: one GPT-175B-shaped parallel block as a ZeRO-2 shard
+(d=12288, ffn=49152; 1,811,963,904 fp32 params, bf16 grads, t=1000, global
+clip 1.0).  A step is one call of the library's ``lamb_step`` (grad-norm,
+moments and apply kernels, plus the result readback).
+
+Prints one JSON line on rank 0:
+  value      params/s over all ranks with every input resident in HBM
+  e2e        the same metric with each step's grads copied from pinned host
+             memory inside the timed region (and the result read back)
+  roofline   the moments kernel (the largest of the three): algorithmic bytes
+             per launch / its CUDA-event duration against the measured HBM peak
+  cpu_baseline  the CPU oracle timed on the host cores on a bounded sample
+
+``--impl reference`` times the CPU oracle instead (on rank 0 only).
+Multi-GPU runs (torchrun) give every rank its own shard: replicas, no
+collective on the data path, weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LAMB step params/s and achieved HBM GB/s (% of GB300 peak), 175B-layer shard"
+UNIT = "params/s"
+# Algorithmic HBM bytes per parameter of each kernel (16-bit grads, fp32 w/m/v,
+# bf16 weight copy): grad norm reads g; moments reads g, m, v, w and writes m, v;
+# apply reads m, v, w and writes w and the bf16 copy.
+BYTES_PER_PARAM = {"grad_norm": 2, "moments": 22, "apply": 18}
+FLOOR_BYTES_PER_PARAM = 28  # g read + w/m/v read and write + bf16 write
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCE = os.path.join(ROOT, "optimizer_step_gb300", "csrc", "lamb_kernels.cu")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--config", default="shard175b",
+                   help="workload: shard175b (default), tiny, ragged, 7b, fp16")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU oracle budget for the cpu_baseline sample")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str) -> None:
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, init_method="env://")
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself on one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, steps: int, world: int, max_seconds: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * steps * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- the peaks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_per_launch(kernel: str, n_params: int):
+    """DRAM bytes of one launch from the committed ncu summary, scaled to
+    n_params, or None when the kernel source changed since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    per = rec.get("dram_bytes_per_param", {}).get(kernel)
+    return None if per is None else float(per) * n_params
+
+
+# ----------------------------------------------------------- CPU baseline
+def cpu_sample(wl, max_elems: int):
+    import workloads as W
+    return W.scaled(wl, max_elems)
+
+
+def time_oracle(wl, steps: int, warmup: int, budget_s: float, max_elems: int):
+    """Times the CPU oracle on a scaled sample of the workload.  Returns
+    (params/s, sample description, threads, steps run, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads as W
+    sw = cpu_sample(wl, max_elems)
+    st = W.make_state(sw, "cpu")
+    host = [[x.numpy() for x in st.w], [x.numpy() for x in st.m], [x.numpy() for x in st.v],
+            [W.as_bits(x).copy() for x in st.w16]]
+    _, gv = W.make_grads(sw, 1, "cpu")
+    g = [W.as_bits(x).copy() for x in gv]
+    gd = oracle.GRAD_FP16 if sw.grad_dtype == torch.float16 else oracle.GRAD_BF16
+    f32 = lambda x: float(np.float32(x))
+    kw = dict(grad_dtype=gd, beta1=f32(sw.beta1), beta2=f32(sw.beta2), eps=f32(sw.eps),
+              weight_decay=f32(sw.weight_decay), lr=f32(sw.lr), clip=f32(sw.clip),
+              loss_scale=f32(sw.loss_scale))
+    t = sw.t0
+    for _ in range(warmup):
+        oracle.lamb_step(*host, g, sw.wd_flags, t=t, **kw)
+        t += 1
+    done, t0 = 0, time.perf_counter()
+    while done < steps and (done == 0 or time.perf_counter() - t0 < budget_s):
+        oracle.lamb_step(*host, g, sw.wd_flags, t=t, **kw)
+        t += 1
+        done += 1
+    el = time.perf_counter() - t0
+    threads = os.cpu_count() or 1
+    desc = (f"{sw.n_params:,} params: every tensor of the workload cut to at most {max_elems:,} "
+            f"elements ({len(sw.sizes)} tensors), {done} timed oracle steps")
+    return sw.n_params * done / el, desc, threads, done, el
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    import workloads as W
+    from optimizer_step_gb300 import Lamb
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    device = torch.device("cuda", local)
+    wl = W.CONFIGS[args.config]()
+    N = wl.n_params
+    st = W.make_state(wl, device)
+    gflat, gv = W.make_grads(wl, 1, device)
+    opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, beta1=wl.beta1, beta2=wl.beta2,
+               eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype)
+    opt.set_grads(gv)
+    opt.set_timing(True)
+    stream = opt.stream
+    t = wl.t0
+
+    def step():
+        nonlocal t
+        sk, _ = opt.step(wl.lr, t, wl.clip, wl.loss_scale)
+        if not sk:
+            t += 1
+        return sk
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    # ---- device-resident timed region
+    sampler = ClockSampler(local)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ktimes = []
+    skips = 0
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        skips += int(step())
+        ktimes.append(opt.kernel_times())
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+    value = whole_job_rate(N, args.steps, world, sec)
+
+    kern = {}
+    for j, name in enumerate(("grad_norm", "moments", "apply")):
+        ms = statistics.mean(k[j] for k in ktimes)
+        gbs = BYTES_PER_PARAM[name] * N / (ms / 1e3) / 1e9
+        kern[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                      "bytes_per_param": BYTES_PER_PARAM[name]}
+    peak, peak_kind = hbm_peak()
+    step_ms = sec / args.steps * 1e3
+    dominant = "moments"
+    achieved = kern[dominant]["GB/s"]
+    traffic = traffic_per_launch(dominant, N)
+
+    # ---- end to end: grads from pinned host memory each step
+    e2e = None
+    if not args.no_e2e:
+        pinned = gflat.cpu().pin_memory()
+        torch.cuda.synchronize()
+        barrier(world)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                gflat.copy_(pinned, non_blocking=True)
+                step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        sec_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+        e2e = {"value": whole_job_rate(N, args.steps, world, sec_e2e), "unit": UNIT,
+               "h2d_bytes_per_step": int(gflat.numel() * gflat.element_size()),
+               "d2h_bytes_per_step": 24, "ms_per_step": round(sec_e2e / args.steps * 1e3, 3)}
+        del pinned
+
+    opt.close()
+    del st, gflat, gv
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, threads, _, _ = time_oracle(wl, 1000, 1, args.cpu_seconds, 1 << 22)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.description, "name": wl.name, "n_params": N,
+                       "tensors": len(wl.sizes), "grad_dtype": str(wl.grad_dtype).split(".")[-1],
+                       "t0": wl.t0, "clip": wl.clip, "loss_scale": wl.loss_scale,
+                       "parallelism": f"replicas x{world} (one shard per GPU, no collective)",
+                       "l2": f"no flush: inputs larger than L2 ({42 * N / 1e9:.1f} GB moved "
+                             f"per step vs 129 MB L2)"},
+            "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes": BYTES_PER_PARAM[dominant] * N},
+            "kernels": kern,
+            "step_hbm": {"bytes_per_param": sum(BYTES_PER_PARAM.values()),
+                         "GB/s": round(sum(BYTES_PER_PARAM.values()) * N / (step_ms / 1e3) / 1e9,
+                                       1),
+                         "frac_of_peak": round(sum(BYTES_PER_PARAM.values()) * N /
+                                               (step_ms / 1e3) / 1e9 / peak, 4),
+                         "floor_28B_GB/s": round(FLOOR_BYTES_PER_PARAM * N / (step_ms / 1e3) /
+                                                 1e9, 1)},
+            "gpu_launches": 3 * args.steps,
+            "skipped_steps": skips,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    import workloads as W
+    wl = W.CONFIGS[args.config]()
+    rate, desc, threads, done, el = time_oracle(wl, args.steps, args.warmup, 1e9, 1 << 22)
+    cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+    out = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
+           "steps": done, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": wl.description, "name": wl.name, "n_params": wl.n_params,
+                      "sample": desc},
+           "cpu_baseline": cpu,
+           "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

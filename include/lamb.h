@@ -1,0 +1,207 @@
+/*
+ * lamb.h -- C ABI of the GB300 (sm_103a) LAMB optimizer-step library.
+ *
+ * One call of lamb_step() performs one LAMB optimizer step on one
+ * data-parallel rank's ZeRO-2 shard of optimizer state, on one GPU.
+ *
+ * The method.  LAMB (You, Li, Reddi et al., "Large Batch Optimization for
+ * Deep Learning: Training BERT in 76 minutes", ICLR 2020) is Adam with a
+ * per-tensor ("layer-wise") trust ratio.  MegaScale adopts it so the batch can
+ * grow 4x without losing accuracy ("MegaScale: Scaling Large Language Model
+ * Training to More Than 10,000 GPUs", guided-reading digest, section 2: LAMB
+ * adapts the learning rate per layer; the same digest's section 8, Table 3,
+ * credits it with +3.0 MFU points).  The state it updates is the rank's ZeRO-2
+ * shard (digest section 3, "Data parallelism (ZeRO-2 style)", and the "Terms"
+ * entry for ZeRO-2: optimizer state and gradients sharded over the
+ * data-parallel ranks).  For tensor i with n_i elements, at step t:
+ *
+ *   per element   g' = c * g / S                       (S: loss scale)
+ *                 m  = b1 m + (1 - b1) g'
+ *                 v  = b2 v + (1 - b2) g'^2
+ *                 r  = (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps) + wd_i w
+ *   per tensor    trust_i = ||w|| / ||r||, or 1 if either norm is 0
+ *                 (||w|| over the weights before the update)
+ *                 w  = w - lr * trust_i * r ;   w16 = bf16_round_nearest_even(w)
+ *   global        G = ||g / S|| over every tensor of the shard (the reported
+ *                 grad norm, before clipping); c = clip / G if clip > 0 and
+ *                 G > clip, else 1; any inf/NaN grad skips the whole step.
+ *
+ * Memory.  Every state and grad buffer lives in device memory, is allocated
+ * and owned by the caller (for example as torch tensors) and must stay valid
+ * for the life of the handle (state) or until lamb_step returns (grads).  The
+ * handle owns only its work table and a small device scratch area (one fp64
+ * and one fp64 pair per work item, two words per tensor, a few scalars) plus
+ * a small pinned host area; lamb_destroy frees them.
+ *
+ * Threads and streams.  A handle is bound to the device that was current at
+ * lamb_create and to the stream given there; every call enqueues its work on
+ * that stream.  A handle must not be used from two host threads at once.
+ *
+ * Errors.  Every int-returning call returns LAMB_OK (0) or a negative code;
+ * lamb_last_error() then gives a message for the calling thread.
+ */
+#ifndef LAMB_GB300_H
+#define LAMB_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LAMB_API __attribute__((visibility("default")))
+#else
+#define LAMB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define LAMB_OK 0
+#define LAMB_ERR_INVALID (-1) /* bad argument: NULL, negative size, t < 1, ... */
+#define LAMB_ERR_ALIGN (-2)   /* a device pointer is not 16-byte aligned */
+#define LAMB_ERR_CUDA (-3)    /* a CUDA runtime call or a kernel launch failed */
+#define LAMB_ERR_NOMEM (-4)   /* device or pinned host allocation failed */
+
+/* Grad element types (all grads of one handle have the same type). */
+#define LAMB_GRAD_BF16 0
+#define LAMB_GRAD_FP16 1
+
+typedef struct lamb_handle lamb_handle;
+
+/* Hyperparameters fixed for the life of a handle.
+ *   beta1, beta2  moment decay rates, each in [0, 1)
+ *   eps           added to sqrt of the corrected second moment, >= 0
+ *   weight_decay  wd applied to tensors whose wd flag is 1, >= 0
+ *   grad_dtype    LAMB_GRAD_BF16 or LAMB_GRAD_FP16 */
+typedef struct {
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  int32_t grad_dtype;
+} lamb_hparams;
+
+/* Outcome of one step.
+ *   skipped    1 if some grad was inf or NaN; the step then wrote nothing
+ *              (w, m, v and w16 are bit-identical to before) and the caller
+ *              should not advance t; 0 otherwise
+ *   grad_norm  ||g / S|| over the whole shard, before clipping; +inf when
+ *              skipped */
+typedef struct {
+  int32_t skipped;
+  int32_t reserved;
+  double grad_norm;
+} lamb_result;
+
+/* One entry of the multi-tensor work table (see lamb_plan).
+ *   tensor >= 0: elements [begin, begin + count) of that tensor;
+ *   tensor == -1: a pack of whole small tensors, whose ids are
+ *                 pack_ids[begin .. begin + count). */
+typedef struct {
+  int64_t begin;
+  int32_t count;
+  int32_t tensor;
+} lamb_work_item;
+
+/*
+ * Create a handle over n_tensors tensors (n_tensors >= 0).
+ *
+ *   sizes[i]     element count of tensor i (>= 0; host array)
+ *   wd_flags[i]  1 if tensor i takes weight decay, 0 if not (for example
+ *                LayerNorm gains and biases); host array
+ *   w[i], m[i], v[i]  device pointers to tensor i's fp32 master weights and
+ *                first / second moments (updated in place by lamb_step)
+ *   w_bf16[i]    device pointer to tensor i's bf16 weight copy (written by
+ *                lamb_step)
+ *   hp           hyperparameters (host struct, copied)
+ *   stream       the cudaStream_t every call enqueues on (NULL: the legacy
+ *                default stream)
+ *
+ * The four pointer arrays are host arrays of device pointers; each pointer of
+ * a non-empty tensor must be non-NULL and 16-byte aligned (LAMB_ERR_ALIGN
+ * otherwise).  The work table is built, uploaded and the call returns after
+ * the uploads complete.  On success *out receives the handle.
+ */
+LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
+                         const uint8_t* wd_flags, float* const* w, float* const* m,
+                         float* const* v, uint16_t* const* w_bf16, const lamb_hparams* hp,
+                         void* stream);
+
+/*
+ * One LAMB step.
+ *
+ *   grads       host array of n_tensors device pointers to this step's grads
+ *               (grad_dtype elements, 16-byte aligned, read only)
+ *   lr          learning rate (finite)
+ *   t           step number, >= 1 (bias corrections use b1^t and b2^t)
+ *   clip        global grad-norm clip threshold; <= 0 disables clipping
+ *   loss_scale  S > 0 (finite); grads are divided by S
+ *   out         receives {skipped, grad_norm}
+ *
+ * Enqueues three kernels on the handle's stream (grad norm, moments and
+ * per-tensor norms, apply), then copies the 24-byte outcome record to pinned host
+ * memory and waits for it: the call returns when the step has finished on
+ * the GPU.  The skip decision is taken on the GPU; the host never reads it in
+ * the middle of a step.
+ */
+LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
+                       float loss_scale, lamb_result* out);
+
+/* Free everything the handle owns (after waiting for its stream).  NULL is a
+ * no-op.  Caller-owned buffers are untouched. */
+LAMB_API int lamb_destroy(lamb_handle* h);
+
+/* Message for the last non-zero return on the calling thread ("" if none).
+ * The pointer stays valid until the next call on this thread. */
+LAMB_API const char* lamb_last_error(void);
+
+/* Diagnostic: copy the per-tensor trust ratios of the last step that was not
+ * skipped into host_out[0 .. n_tensors) (1.0 for empty tensors and before the
+ * first step).  Waits for the handle's stream. */
+LAMB_API int lamb_get_trust(lamb_handle* h, float* host_out, int32_t n_tensors);
+
+/*
+ * CUDA event monitor (after the per-rank CUDA-event timing of MegaScale's
+ * guided-reading digest, section 7: critical segments are timed with CUDA
+ * events instead of host timers, so timing forces no synchronisation and can
+ * stay on).  With timing enabled, lamb_step records an event before its first
+ * kernel and after each of its three kernels, on the handle's stream.
+ *
+ *   lamb_set_timing    enable != 0 turns the monitor on (creating the events),
+ *                      0 turns it off
+ *   lamb_kernel_times  ms[0..3) receive the device durations, in
+ *                      milliseconds, of the last step's grad-norm, moments
+ *                      and apply kernels (LAMB_ERR_INVALID if the monitor is
+ *                      off or no step has run since it was turned on)
+ */
+LAMB_API int lamb_set_timing(lamb_handle* h, int32_t enable);
+LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms);
+
+/*
+ * Host-only view of the work table lamb_create builds (no GPU needed).
+ *
+ * Tensors larger than small_max elements are split into chunks of at most
+ * chunk_elems elements whose starts are multiples of 8 elements; tensors of
+ * 1 .. small_max elements are packed whole, in order, into packs of at most
+ * pack_budget elements and pack_max tensors; empty tensors get no work.
+ *
+ *   items, items_cap        output array for the work items (may be NULL)
+ *   pack_ids, pack_cap      output array for packed tensor ids (may be NULL)
+ *   n_items, n_pack_ids     receive the full counts
+ *
+ * Returns LAMB_ERR_INVALID (with the counts still set) when a capacity is too
+ * small for a non-NULL output array.
+ */
+LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, lamb_work_item* items,
+                       int64_t items_cap, int32_t* pack_ids, int64_t pack_cap, int64_t* n_items,
+                       int64_t* n_pack_ids);
+
+/* The constants lamb_plan uses (any output may be NULL). */
+LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* small_max, int64_t* pack_budget,
+                               int64_t* pack_max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAMB_GB300_H */

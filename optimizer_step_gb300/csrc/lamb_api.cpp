@@ -1,0 +1,379 @@
+// C ABI of the LAMB step library: argument checks, the handle's device and
+// pinned memory, and the per-step launch sequence.  The interface contract is
+// documented in include/lamb.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "lamb_internal.h"
+
+using namespace lambgb;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? LAMB_ERR_NOMEM : LAMB_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) +
+                  ")");
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Makes the handle's device current for the duration of a call and restores
+// the caller's device afterwards.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct lamb_handle {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  lamb_hparams hp{};
+  int32_t n_tensors = 0;
+  Plan plan;
+  std::vector<int64_t> sizes;
+  void* dev_block = nullptr;       // every device table and scratch array
+  void* pinned = nullptr;          // grads staging + step scalars readback
+  const void** grads_stage = nullptr;
+  StepScalars* scalars_host = nullptr;
+  std::vector<const void*> grads_cached;
+  bool grads_uploaded = false;
+  DevTables T{};
+  int grid[3] = {0, 0, 0};
+  bool timing = false;        // CUDA event monitor on
+  bool timed_step = false;    // a step has been timed since it was turned on
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+
+namespace {
+
+void destroy_events(lamb_handle* h) {
+  for (auto& e : h->ev) {
+    if (e) cudaEventDestroy(e);
+    e = nullptr;
+  }
+  h->timing = false;
+  h->timed_step = false;
+}
+
+// Records monitor event k on the handle's stream (no-op when timing is off).
+cudaError_t mark(lamb_handle* h, int k) {
+  return h->timing ? cudaEventRecord(h->ev[k], h->stream) : cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+LAMB_API const char* lamb_last_error(void) { return g_last_error.c_str(); }
+
+LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
+                         const uint8_t* wd_flags, float* const* w, float* const* m,
+                         float* const* v, uint16_t* const* w_bf16, const lamb_hparams* hp,
+                         void* stream) {
+  g_last_error.clear();
+  if (!out) return fail(LAMB_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (!hp) return fail(LAMB_ERR_INVALID, "hparams is NULL");
+  if (n_tensors < 0) return fail(LAMB_ERR_INVALID, "n_tensors must be >= 0");
+  if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+    return fail(LAMB_ERR_INVALID, "beta1 and beta2 must lie in [0, 1)");
+  if (!(hp->eps >= 0.0f) || !std::isfinite(hp->eps))
+    return fail(LAMB_ERR_INVALID, "eps must be finite and >= 0");
+  if (!(hp->weight_decay >= 0.0f) || !std::isfinite(hp->weight_decay))
+    return fail(LAMB_ERR_INVALID, "weight_decay must be finite and >= 0");
+  if (hp->grad_dtype != LAMB_GRAD_BF16 && hp->grad_dtype != LAMB_GRAD_FP16)
+    return fail(LAMB_ERR_INVALID, "grad_dtype must be LAMB_GRAD_BF16 or LAMB_GRAD_FP16");
+  if (n_tensors > 0 && (!sizes || !wd_flags || !w || !m || !v || !w_bf16))
+    return fail(LAMB_ERR_INVALID, "sizes, wd_flags and the pointer arrays must be non-NULL");
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    if (sizes[i] < 0) return fail(LAMB_ERR_INVALID, "sizes[" + std::to_string(i) + "] < 0");
+    if (sizes[i] == 0) continue;
+    if (!w[i] || !m[i] || !v[i] || !w_bf16[i])
+      return fail(LAMB_ERR_INVALID, "tensor " + std::to_string(i) + " has a NULL pointer");
+    if (!aligned16(w[i]) || !aligned16(m[i]) || !aligned16(v[i]) || !aligned16(w_bf16[i]))
+      return fail(LAMB_ERR_ALIGN,
+                  "tensor " + std::to_string(i) + " has a pointer not 16-byte aligned");
+  }
+
+  lamb_handle* h = new (std::nothrow) lamb_handle();
+  if (!h) return fail(LAMB_ERR_NOMEM, "host allocation failed");
+  std::string err;
+  if (!build_plan(n_tensors, sizes, &h->plan, &err)) {
+    delete h;
+    return fail(LAMB_ERR_INVALID, err);
+  }
+  h->n_tensors = n_tensors;
+  h->hp = *hp;
+  h->stream = static_cast<cudaStream_t>(stream);
+  h->sizes.assign(sizes, sizes + n_tensors);
+  cudaError_t ce = cudaGetDevice(&h->device);
+  if (ce != cudaSuccess) {
+    delete h;
+    return cuda_fail(ce, "cudaGetDevice");
+  }
+
+  // Host copies of the per-tensor records.
+  const size_t nt = size_t(n_tensors), ni = h->plan.items.size(), np = h->plan.pack_ids.size();
+  std::vector<TensorDesc> td(nt);
+  for (size_t i = 0; i < nt; ++i) {
+    td[i].w = w[i];
+    td[i].m = m[i];
+    td[i].v = v[i];
+    td[i].w16 = w_bf16[i];
+    td[i].n = sizes[i];
+    td[i].wd = wd_flags[i] ? hp->weight_decay : 0.0f;
+    td[i].first_item = h->plan.first_item[i];
+    td[i].n_items = h->plan.n_items[i];
+    td[i].pad = 0;
+  }
+  std::vector<float> ones(nt, 1.0f);
+
+  // One device allocation, carved into 256-byte aligned regions.
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + std::max<size_t>(bytes, 1), 256);
+    return at;
+  };
+  const size_t o_td = carve(nt * sizeof(TensorDesc));
+  const size_t o_items = carve(ni * sizeof(lamb_work_item));
+  const size_t o_pack = carve(np * sizeof(int32_t));
+  const size_t o_grads = carve(nt * sizeof(void*));
+  const size_t o_g2 = carve(ni * sizeof(double));
+  const size_t o_wr = carve(ni * sizeof(double2));
+  const size_t o_ticket = carve(nt * sizeof(uint32_t));
+  const size_t o_trust = carve(nt * sizeof(float));
+  const size_t o_sc = carve(sizeof(StepScalars));
+  ce = cudaMalloc(&h->dev_block, off);
+  if (ce != cudaSuccess) {
+    delete h;
+    return cuda_fail(ce, "cudaMalloc of the work table");
+  }
+  ce = cudaMallocHost(&h->pinned, round_up(nt * sizeof(void*), 256) + sizeof(StepScalars));
+  if (ce != cudaSuccess) {
+    cudaFree(h->dev_block);
+    delete h;
+    return cuda_fail(ce, "cudaMallocHost");
+  }
+  char* base = static_cast<char*>(h->dev_block);
+  h->grads_stage = static_cast<const void**>(h->pinned);
+  h->scalars_host = reinterpret_cast<StepScalars*>(static_cast<char*>(h->pinned) +
+                                                   round_up(nt * sizeof(void*), 256));
+  DevTables& T = h->T;
+  T.td = reinterpret_cast<const TensorDesc*>(base + o_td);
+  T.items = reinterpret_cast<const lamb_work_item*>(base + o_items);
+  T.pack_ids = reinterpret_cast<const int32_t*>(base + o_pack);
+  T.grads = reinterpret_cast<const void* const*>(base + o_grads);
+  T.item_g2 = reinterpret_cast<double*>(base + o_g2);
+  T.item_wr = reinterpret_cast<double2*>(base + o_wr);
+  T.tensor_ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
+  T.trust = reinterpret_cast<float*>(base + o_trust);
+  T.sc = reinterpret_cast<StepScalars*>(base + o_sc);
+  T.n_items = int32_t(ni);
+
+  auto up = [&](size_t o, const void* src, size_t bytes) {
+    return bytes ? cudaMemcpyAsync(base + o, src, bytes, cudaMemcpyHostToDevice, h->stream)
+                 : cudaSuccess;
+  };
+  if ((ce = cudaMemsetAsync(h->dev_block, 0, off, h->stream)) != cudaSuccess ||
+      (ce = up(o_td, td.data(), nt * sizeof(TensorDesc))) != cudaSuccess ||
+      (ce = up(o_items, h->plan.items.data(), ni * sizeof(lamb_work_item))) != cudaSuccess ||
+      (ce = up(o_pack, h->plan.pack_ids.data(), np * sizeof(int32_t))) != cudaSuccess ||
+      (ce = up(o_trust, ones.data(), nt * sizeof(float))) != cudaSuccess ||
+      (ce = cudaStreamSynchronize(h->stream)) != cudaSuccess) {
+    cudaFreeHost(h->pinned);
+    cudaFree(h->dev_block);
+    delete h;
+    return cuda_fail(ce, "uploading the work table");
+  }
+
+  // Persistent grids: as many CTAs as fit at once, never more than the items.
+  int sms = 0;
+  ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (ce != cudaSuccess) {
+    cudaFreeHost(h->pinned);
+    cudaFree(h->dev_block);
+    delete h;
+    return cuda_fail(ce, "cudaDeviceGetAttribute");
+  }
+  for (int k = 0; k < 3; ++k) {
+    int per_sm = max_blocks_per_sm(k, hp->grad_dtype);
+    if (per_sm <= 0) {
+      cudaFreeHost(h->pinned);
+      cudaFree(h->dev_block);
+      delete h;
+      return cuda_fail(per_sm < 0 ? cudaError_t(-per_sm) : cudaErrorInvalidConfiguration,
+                       "occupancy query");
+    }
+    const int64_t full = int64_t(per_sm) * sms;
+    h->grid[k] = int(std::max<int64_t>(1, std::min<int64_t>(full, int64_t(ni))));
+  }
+  *out = h;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
+                       float loss_scale, lamb_result* out) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (!out) return fail(LAMB_ERR_INVALID, "out is NULL");
+  if (t < 1) return fail(LAMB_ERR_INVALID, "t must be >= 1");
+  if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+    return fail(LAMB_ERR_INVALID, "loss_scale must be finite and > 0");
+  if (!std::isfinite(lr)) return fail(LAMB_ERR_INVALID, "lr must be finite");
+  if (std::isnan(clip)) return fail(LAMB_ERR_INVALID, "clip is NaN");
+  if (h->n_tensors > 0 && !grads) return fail(LAMB_ERR_INVALID, "grads is NULL");
+  for (int32_t i = 0; i < h->n_tensors; ++i) {
+    if (h->sizes[size_t(i)] == 0) continue;
+    if (!grads[i]) return fail(LAMB_ERR_INVALID, "grads[" + std::to_string(i) + "] is NULL");
+    if (!aligned16(grads[i]))
+      return fail(LAMB_ERR_ALIGN, "grads[" + std::to_string(i) + "] is not 16-byte aligned");
+  }
+  out->skipped = 0;
+  out->reserved = 0;
+  out->grad_norm = 0.0;
+  if (h->T.n_items == 0) return LAMB_OK;  // nothing to update: norm 0, no skip
+
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  cudaError_t ce;
+  const size_t nt = size_t(h->n_tensors);
+  if (!h->grads_uploaded ||
+      std::memcmp(h->grads_cached.data(), grads, nt * sizeof(void*)) != 0) {
+    // The staging area is free: every earlier step waited for its stream.
+    std::memcpy(h->grads_stage, grads, nt * sizeof(void*));
+    ce = cudaMemcpyAsync(const_cast<const void**>(h->T.grads), h->grads_stage,
+                         nt * sizeof(void*), cudaMemcpyHostToDevice, h->stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "uploading grad pointers");
+    h->grads_cached.assign(grads, grads + nt);
+    h->grads_uploaded = true;
+  }
+
+  const double b1 = h->hp.beta1, b2 = h->hp.beta2;
+  Hyper hy;
+  hy.b1 = h->hp.beta1;
+  hy.b2 = h->hp.beta2;
+  hy.omb1 = float(1.0 - b1);
+  hy.omb2 = float(1.0 - b2);
+  hy.c1 = float(1.0 / (1.0 - std::pow(b1, double(t))));
+  hy.c2 = float(1.0 / (1.0 - std::pow(b2, double(t))));
+  hy.eps = h->hp.eps;
+  hy.lr = lr;
+
+  if ((ce = mark(h, 0)) != cudaSuccess) return cuda_fail(ce, "event record");
+  int rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, clip, double(loss_scale),
+                            h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
+  if ((ce = mark(h, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
+  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
+  if ((ce = mark(h, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
+  rc = launch_apply(h->T, h->grid[2], hy, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+  if ((ce = mark(h, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
+  ce = cudaMemcpyAsync(h->scalars_host, h->T.sc, sizeof(StepScalars), cudaMemcpyDeviceToHost,
+                       h->stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "reading the step result");
+  ce = cudaStreamSynchronize(h->stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the step");
+  out->skipped = h->scalars_host->skip;
+  out->grad_norm = h->scalars_host->grad_norm;
+  if (h->timing) h->timed_step = true;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_set_timing(lamb_handle* h, int32_t enable) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  if (!enable) {
+    cudaError_t ce = cudaStreamSynchronize(h->stream);
+    destroy_events(h);
+    return ce == cudaSuccess ? LAMB_OK : cuda_fail(ce, "waiting for the stream");
+  }
+  if (h->timing) return LAMB_OK;
+  for (auto& e : h->ev) {
+    cudaError_t ce = cudaEventCreate(&e);
+    if (ce != cudaSuccess) {
+      destroy_events(h);
+      return cuda_fail(ce, "cudaEventCreate");
+    }
+  }
+  h->timing = true;
+  h->timed_step = false;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms) {
+  g_last_error.clear();
+  if (!h || !ms) return fail(LAMB_ERR_INVALID, "NULL argument");
+  if (!h->timing || !h->timed_step)
+    return fail(LAMB_ERR_INVALID, "no timed step: enable the monitor and run a step first");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  for (int k = 0; k < 3; ++k) {
+    cudaError_t ce = cudaEventSynchronize(h->ev[k + 1]);
+    if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms[k], h->ev[k], h->ev[k + 1]);
+    if (ce != cudaSuccess) return cuda_fail(ce, "reading monitor events");
+  }
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_get_trust(lamb_handle* h, float* host_out, int32_t n_tensors) {
+  g_last_error.clear();
+  if (!h || !host_out) return fail(LAMB_ERR_INVALID, "NULL argument");
+  if (n_tensors != h->n_tensors) return fail(LAMB_ERR_INVALID, "n_tensors does not match");
+  if (n_tensors == 0) return LAMB_OK;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  cudaError_t ce = cudaStreamSynchronize(h->stream);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpy(host_out, h->T.trust, size_t(n_tensors) * sizeof(float),
+                    cudaMemcpyDeviceToHost);
+  return ce == cudaSuccess ? LAMB_OK : cuda_fail(ce, "reading trust ratios");
+}
+
+LAMB_API int lamb_destroy(lamb_handle* h) {
+  g_last_error.clear();
+  if (!h) return LAMB_OK;
+  int rc = LAMB_OK;
+  {
+    DeviceGuard dg(h->device);
+    cudaError_t ce = cudaStreamSynchronize(h->stream);
+    if (ce != cudaSuccess) rc = cuda_fail(ce, "waiting for the stream");
+    destroy_events(h);
+    if (h->pinned) cudaFreeHost(h->pinned);
+    if (h->dev_block) cudaFree(h->dev_block);
+  }
+  delete h;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Internal declarations shared by the host side (plan builder, C ABI) and the
+// kernels of the LAMB step library.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <vector_types.h>
+
+#include "lamb.h"
+
+namespace lambgb {
+
+// Work-table shape.  Large tensors are cut into chunks of at most kChunkElems
+// elements (multiples of 8, so every chunk start keeps 16-byte alignment of
+// the fp32 and 16-bit arrays); tensors up to kSmallMax elements are packed
+// whole, one warp per tensor, kPackBudget elements / kPackMax tensors a pack.
+constexpr int64_t kChunkElems = 32768;
+constexpr int64_t kSmallMax = 4096;
+constexpr int64_t kPackBudget = 32768;
+constexpr int64_t kPackMax = 256;
+
+struct Plan {
+  std::vector<lamb_work_item> items;
+  std::vector<int32_t> pack_ids;
+  std::vector<int32_t> first_item;  // per tensor: index of its first chunk item (-1: packed/empty)
+  std::vector<int32_t> n_items;     // per tensor: number of chunk items (0: packed/empty)
+};
+
+// Builds the work table; returns false (with a message) on invalid sizes or
+// a table too large for 32-bit item indices.
+bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string* err);
+
+// Per-tensor record the kernels read (device copy built at create time).
+struct TensorDesc {
+  float* w;
+  float* m;
+  float* v;
+  uint16_t* w16;
+  int64_t n;
+  float wd;            // weight_decay if the tensor's flag is set, else 0
+  int32_t first_item;  // first chunk item of a chunked tensor
+  int32_t n_items;     // number of chunk items (0 for packed tensors)
+  int32_t pad;
+};
+
+// Device-resident values of one step, written by the grad-norm kernel's last
+// CTA and read by the two later kernels and by the host.
+struct StepScalars {
+  double grad_norm;    // ||g / S|| (+inf if skipped)
+  float gscale;        // c / S, the factor turning a raw grad into g'
+  int32_t skip;        // 1: a grad was inf/NaN, nothing is written
+  uint32_t ticket;     // CTAs of the grad-norm kernel that have finished
+  uint32_t nonfinite;  // OR of every CTA's inf/NaN flag
+};
+
+// Device pointers of one handle, passed by value to every kernel.
+struct DevTables {
+  const lamb_work_item* items;
+  const int32_t* pack_ids;
+  const TensorDesc* td;
+  const void* const* grads;  // per-step grad pointers (device array)
+  double* item_g2;           // per work item: sum of raw g^2
+  double2* item_wr;          // per chunk item: (sum w^2, sum r^2)
+  uint32_t* tensor_ticket;   // per tensor: chunk items finished this step
+  float* trust;              // per tensor: trust ratio of this step
+  StepScalars* sc;
+  int32_t n_items;
+};
+
+struct Hyper {
+  float b1, b2, omb1, omb2;  // beta1, beta2, 1-beta1, 1-beta2
+  float c1, c2;              // 1/(1-beta1^t), 1/(1-beta2^t)
+  float eps, lr;
+};
+
+// Kernel launchers (lamb_kernels.cu).  Each returns the launch's error code.
+int max_blocks_per_sm(int kernel, int grad_dtype);  // kernel: 0 norm, 1 moments, 2 apply
+int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip, double loss_scale,
+                     void* stream);
+int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream);
+int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream);
+
+}  // namespace lambgb

@@ -1,0 +1,477 @@
+// The three kernels of one LAMB step on sm_103a.
+//
+// LAMB (You et al., ICLR 2020) as adopted by MegaScale ("MegaScale: Scaling
+// Large Language Model Training to More Than 10,000 GPUs", guided-reading
+// digest, section 2: per-layer learning-rate adaptation), on one rank's ZeRO-2
+// shard (digest section 3).  The step is purely memory-bound (about 25 flops,
+// one sqrt and one divide per element against 42 bytes), so there is no
+// tensor-core work here: what matters is coalesced 128-bit traffic, enough
+// bytes in flight per SM, and no extra passes over HBM.
+//
+// The exact method needs three passes, because r needs the global clip factor
+// and the update needs the whole tensor's ||r||:
+//   A  grad_norm_kernel  reads g (2 B/elem): sum of g^2, inf/NaN flag; its
+//      last CTA (atomic ticket, no waiting) forms ||g/S||, the clip factor and
+//      the skip flag on the device.
+//   B  moments_kernel    reads g, m, v, w and writes m, v (22 B/elem); forms
+//      per-tensor sum w^2 and sum r^2; the last CTA of each tensor (ticket)
+//      turns them into trust_i.
+//   C  apply_kernel      reads m, v, w and writes w and the bf16 copy
+//      (18 B/elem); r is recomputed with the same function as in B, so the r
+//      applied is bit-identical to the r whose norm was taken.
+// Recomputing r costs the same bytes as storing it (B +4 B write, C reads r
+// instead of m and v), and avoids a 4 B/param scratch buffer.
+//
+// Work is split by the host-built table of work items (chunks of large
+// tensors; packs of small tensors, a warp per tensor).  Grids are persistent:
+// each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
+// Every reduction has a fixed order, so results are deterministic run to run.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "lamb_internal.h"
+
+namespace lambgb {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 2;  // 8-element vectors in flight per thread per loop trip
+
+// ------------------------------------------------------------ memory access
+// Everything is streamed once per kernel and the step's footprint is far
+// larger than L2, so loads and stores are marked evict-first (.cs).
+__device__ __forceinline__ uint4 ld_u4(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+  return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void st_f4(float* p, float4 x) {
+  __stcs(reinterpret_cast<float4*>(p), x);
+}
+__device__ __forceinline__ void st_u4(void* p, uint4 x) {
+  __stcs(reinterpret_cast<uint4*>(p), x);
+}
+
+// ----------------------------------------------------------- grad decoding
+// Two 16-bit grads packed in one 32-bit word -> two floats (exact).
+template <int DT>
+__device__ __forceinline__ float2 decode2(uint32_t x);
+template <>
+__device__ __forceinline__ float2 decode2<LAMB_GRAD_BF16>(uint32_t x) {
+  return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ float2 decode2<LAMB_GRAD_FP16>(uint32_t x) {
+  __half2 h;
+  static_assert(sizeof(h) == sizeof(x), "half2 size");
+  memcpy(&h, &x, sizeof x);
+  return __half22float2(h);
+}
+template <int DT>
+__device__ __forceinline__ float decode1(uint16_t x) {
+  return decode2<DT>(uint32_t(x) | (uint32_t(x) << 16)).x;
+}
+
+// 1 if either 16-bit half of x has an all-ones exponent (inf or NaN).
+template <int DT>
+__device__ __forceinline__ uint32_t nonfinite2(uint32_t x) {
+  constexpr uint32_t kExp = DT == LAMB_GRAD_BF16 ? 0x7F807F80u : 0x7C007C00u;
+  const uint32_t u = ~x & kExp;  // a half is 0 here iff its exponent is all ones
+  return uint32_t((u & 0xFFFFu) == 0u) | uint32_t((u >> 16) == 0u);
+}
+
+// -------------------------------------------------------------- reductions
+__device__ __forceinline__ double warp_sum(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Fixed-shape block sum; the result is valid in every thread.
+__device__ __forceinline__ double block_sum(double x, double* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  x = warp_sum(x);
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  double y = lane < kWarps ? red[lane] : 0.0;
+  y = warp_sum(y);
+  __syncthreads();
+  return y;
+}
+
+__device__ __forceinline__ double2 block_sum2(double a, double b, double2* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (lane == 0) red[warp] = make_double2(a, b);
+  __syncthreads();
+  double2 y = lane < kWarps ? red[lane] : make_double2(0.0, 0.0);
+  y.x = warp_sum(y.x);
+  y.y = warp_sum(y.y);
+  __syncthreads();
+  return y;
+}
+
+__device__ __forceinline__ float trust_of(double sum_w2, double sum_r2) {
+  const double wn = sqrt(sum_w2), rn = sqrt(sum_r2);
+  return (wn > 0.0 && rn > 0.0) ? float(wn / rn) : 1.0f;
+}
+
+// ------------------------------------------------------ per-element math
+// Explicitly rounded operations (never contracted), so kernels B and C get
+// bit-identical r from the same stored m, v and w.
+struct Elem {
+  float b1, b2, omb1, omb2, c1, c2, eps, gs;
+  __device__ __forceinline__ void moments(float g, float& m, float& v) const {
+    const float gp = __fmul_rn(g, gs);
+    m = __fmaf_rn(b1, m, __fmul_rn(omb1, gp));
+    v = __fmaf_rn(b2, v, __fmul_rn(omb2, __fmul_rn(gp, gp)));
+  }
+  __device__ __forceinline__ float direction(float m, float v, float w, float wd) const {
+    const float den = __fadd_rn(__fsqrt_rn(__fmul_rn(v, c2)), eps);
+    return __fmaf_rn(wd, w, __fdiv_rn(__fmul_rn(m, c1), den));
+  }
+};
+
+__device__ __forceinline__ float4 get4(const float (&a)[8], int h) {
+  return make_float4(a[4 * h], a[4 * h + 1], a[4 * h + 2], a[4 * h + 3]);
+}
+__device__ __forceinline__ void put4(float (&a)[8], int h, float4 x) {
+  a[4 * h] = x.x;
+  a[4 * h + 1] = x.y;
+  a[4 * h + 2] = x.z;
+  a[4 * h + 3] = x.w;
+}
+
+// ===================================================== A: grad norm pass
+// Sum of raw g^2 and the inf/NaN flag over elements [0, n) of one grad array,
+// thread tid of nthr.
+template <int DT>
+__device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int64_t n, int tid,
+                                            int nthr, float& acc, uint32_t& bad) {
+  const int64_t nv = n >> 3;
+#pragma unroll 4
+  for (int64_t k = tid; k < nv; k += nthr) {
+    const uint4 q = ld_u4(g + 8 * k);
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = decode2<DT>(wv[j]);
+      acc = __fmaf_rn(f.x, f.x, acc);
+      acc = __fmaf_rn(f.y, f.y, acc);
+      bad |= nonfinite2<DT>(wv[j]);
+    }
+  }
+  for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {
+    const uint16_t x = g[j];
+    const float f = decode1<DT>(x);
+    acc = __fmaf_rn(f, f, acc);
+    bad |= nonfinite2<DT>(uint32_t(x) | (uint32_t(x) << 16));
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) grad_norm_kernel(DevTables T, float clip,
+                                                             double loss_scale) {
+  __shared__ double red[kWarps];
+  __shared__ int is_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t bad = 0;
+  for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
+    const lamb_work_item wi = T.items[it];
+    float acc = 0.0f;
+    if (wi.tensor >= 0) {
+      const uint16_t* g = static_cast<const uint16_t*>(T.grads[wi.tensor]) + wi.begin;
+      sumsq_range<DT>(g, wi.count, threadIdx.x, kThreads, acc, bad);
+    } else {
+      for (int k = warp; k < wi.count; k += kWarps) {
+        const int32_t ti = T.pack_ids[wi.begin + k];
+        sumsq_range<DT>(static_cast<const uint16_t*>(T.grads[ti]), T.td[ti].n, lane, 32, acc,
+                        bad);
+      }
+    }
+    const double s = block_sum(double(acc), red);
+    if (threadIdx.x == 0) T.item_g2[it] = s;
+  }
+
+  // Completion ticket: the CTA that finishes last reduces every item's sum in
+  // item order and publishes the step's scalars.  Nobody waits.
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    if (bad) atomicOr(&T.sc->nonfinite, 1u);
+    __threadfence();
+    const uint32_t prev = atomicAdd(&T.sc->ticket, 1u);
+    is_last = prev == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  double s = 0.0;
+  for (int32_t i = threadIdx.x; i < T.n_items; i += kThreads) s += __ldcg(&T.item_g2[i]);
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) {
+    StepScalars* sc = T.sc;
+    const uint32_t nf = atomicExch(&sc->nonfinite, 0u);
+    if (nf) {
+      sc->skip = 1;
+      sc->grad_norm = __longlong_as_double(0x7FF0000000000000ll);  // +inf
+      sc->gscale = 0.0f;
+    } else {
+      const double gn = sqrt(s) / loss_scale;
+      const double c = (clip > 0.0f && gn > double(clip)) ? double(clip) / gn : 1.0;
+      sc->skip = 0;
+      sc->grad_norm = gn;
+      sc->gscale = float(c / loss_scale);
+    }
+    sc->ticket = 0u;  // ready for the next step
+  }
+}
+
+// ================================================ B: moments + norms pass
+template <int DT>
+__device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_t* __restrict__ g,
+                                              int64_t begin, int64_t n, int tid, int nthr,
+                                              const Elem& e, float& sw, float& sr) {
+  float* __restrict__ m = d.m + begin;
+  float* __restrict__ v = d.v + begin;
+  const float* __restrict__ w = d.w + begin;
+  g += begin;
+  const float wd = d.wd;
+  const int64_t nv = n >> 3;
+  for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kUnroll) * nthr) {
+    uint4 gq[kUnroll];
+    float mr[kUnroll][8], vr[kUnroll][8], wr[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t k = k0 + int64_t(u) * nthr;
+      if (k < nv) {
+        gq[u] = ld_u4(g + 8 * k);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          put4(mr[u], h, ld_f4(m + 8 * k + 4 * h));
+          put4(vr[u], h, ld_f4(v + 8 * k + 4 * h));
+          put4(wr[u], h, ld_f4(w + 8 * k + 4 * h));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t k = k0 + int64_t(u) * nthr;
+      if (k < nv) {
+        const uint32_t wv[4] = {gq[u].x, gq[u].y, gq[u].z, gq[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = decode2<DT>(wv[j]);
+          e.moments(f.x, mr[u][2 * j], vr[u][2 * j]);
+          e.moments(f.y, mr[u][2 * j + 1], vr[u][2 * j + 1]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float r = e.direction(mr[u][q], vr[u][q], wr[u][q], wd);
+          sw = __fmaf_rn(wr[u][q], wr[u][q], sw);
+          sr = __fmaf_rn(r, r, sr);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          st_f4(m + 8 * k + 4 * h, get4(mr[u], h));
+          st_f4(v + 8 * k + 4 * h, get4(vr[u], h));
+        }
+      }
+    }
+  }
+  for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {
+    float mj = m[j], vj = v[j];
+    const float wj = w[j];
+    e.moments(decode1<DT>(g[j]), mj, vj);
+    const float r = e.direction(mj, vj, wj, wd);
+    sw = __fmaf_rn(wj, wj, sw);
+    sr = __fmaf_rn(r, r, sr);
+    m[j] = mj;
+    v[j] = vj;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) moments_kernel(DevTables T, Hyper hp) {
+  __shared__ double2 red[kWarps];
+  __shared__ int is_last;
+  const StepScalars* sc = T.sc;
+  if (sc->skip) return;
+  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, sc->gscale};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
+    const lamb_work_item wi = T.items[it];
+    if (wi.tensor >= 0) {
+      const TensorDesc d = T.td[wi.tensor];
+      float sw = 0.0f, sr = 0.0f;
+      moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[wi.tensor]), wi.begin, wi.count,
+                        threadIdx.x, kThreads, e, sw, sr);
+      const double2 s = block_sum2(sw, sr, red);
+      if (d.n_items == 1) {
+        if (threadIdx.x == 0) T.trust[wi.tensor] = trust_of(s.x, s.y);
+        continue;
+      }
+      if (threadIdx.x == 0) {
+        T.item_wr[it] = s;
+        __threadfence();
+        const uint32_t prev = atomicAdd(&T.tensor_ticket[wi.tensor], 1u);
+        is_last = prev == uint32_t(d.n_items - 1);
+      }
+      __syncthreads();
+      if (is_last) {
+        // Last chunk of this tensor: sum its chunks' partials in item order.
+        __threadfence();
+        double a = 0.0, b = 0.0;
+        for (int32_t k = threadIdx.x; k < d.n_items; k += kThreads) {
+          const double2 x = __ldcg(&T.item_wr[d.first_item + k]);
+          a += x.x;
+          b += x.y;
+        }
+        const double2 tot = block_sum2(a, b, red);
+        if (threadIdx.x == 0) {
+          T.trust[wi.tensor] = trust_of(tot.x, tot.y);
+          T.tensor_ticket[wi.tensor] = 0u;
+        }
+      }
+    } else {
+      for (int k = warp; k < wi.count; k += kWarps) {
+        const int32_t ti = T.pack_ids[wi.begin + k];
+        const TensorDesc d = T.td[ti];
+        float sw = 0.0f, sr = 0.0f;
+        moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[ti]), 0, d.n, lane, 32, e, sw,
+                          sr);
+        const double a = warp_sum(double(sw)), b = warp_sum(double(sr));
+        if (lane == 0) T.trust[ti] = trust_of(a, b);
+      }
+    }
+  }
+}
+
+// ========================================================= C: apply pass
+__device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, int64_t n, int tid,
+                                            int nthr, const Elem& e, float step) {
+  const float* __restrict__ m = d.m + begin;
+  const float* __restrict__ v = d.v + begin;
+  float* __restrict__ w = d.w + begin;
+  uint16_t* __restrict__ w16 = d.w16 + begin;
+  const float wd = d.wd;
+  const int64_t nv = n >> 3;
+  for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kUnroll) * nthr) {
+    float mr[kUnroll][8], vr[kUnroll][8], wr[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t k = k0 + int64_t(u) * nthr;
+      if (k < nv) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          put4(mr[u], h, ld_f4(m + 8 * k + 4 * h));
+          put4(vr[u], h, ld_f4(v + 8 * k + 4 * h));
+          put4(wr[u], h, ld_f4(w + 8 * k + 4 * h));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t k = k0 + int64_t(u) * nthr;
+      if (k < nv) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float r = e.direction(mr[u][q], vr[u][q], wr[u][q], wd);
+          wr[u][q] = __fmaf_rn(-step, r, wr[u][q]);
+        }
+        uint32_t packed[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 b2 =
+              __floats2bfloat162_rn(wr[u][2 * j], wr[u][2 * j + 1]);  // .x low half
+          memcpy(&packed[j], &b2, sizeof(uint32_t));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) st_f4(w + 8 * k + 4 * h, get4(wr[u], h));
+        st_u4(w16 + 8 * k, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+      }
+    }
+  }
+  for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {
+    const float r = e.direction(m[j], v[j], w[j], wd);
+    const float wn = __fmaf_rn(-step, r, w[j]);
+    w[j] = wn;
+    const __nv_bfloat16 b = __float2bfloat16_rn(wn);
+    memcpy(&w16[j], &b, sizeof(uint16_t));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) apply_kernel(DevTables T, Hyper hp) {
+  const StepScalars* sc = T.sc;
+  if (sc->skip) return;
+  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, 0.0f};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
+    const lamb_work_item wi = T.items[it];
+    if (wi.tensor >= 0) {
+      const TensorDesc d = T.td[wi.tensor];
+      const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
+      apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
+    } else {
+      for (int k = warp; k < wi.count; k += kWarps) {
+        const int32_t ti = T.pack_ids[wi.begin + k];
+        const TensorDesc d = T.td[ti];
+        apply_range(d, 0, d.n, lane, 32, e, __fmul_rn(hp.lr, T.trust[ti]));
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+int max_blocks_per_sm(int kernel, int grad_dtype) {
+  int nb = 0;
+  cudaError_t err = cudaSuccess;
+  const bool fp16 = grad_dtype == LAMB_GRAD_FP16;
+  if (kernel == 0) {
+    err = fp16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &nb, grad_norm_kernel<LAMB_GRAD_FP16>, kThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &nb, grad_norm_kernel<LAMB_GRAD_BF16>, kThreads, 0);
+  } else if (kernel == 1) {
+    err = fp16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &nb, moments_kernel<LAMB_GRAD_FP16>, kThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &nb, moments_kernel<LAMB_GRAD_BF16>, kThreads, 0);
+  } else {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, apply_kernel, kThreads, 0);
+  }
+  return err == cudaSuccess ? nb : -int(err);
+}
+
+int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip, double loss_scale,
+                     void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (grad_dtype == LAMB_GRAD_FP16)
+    grad_norm_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, clip, loss_scale);
+  else
+    grad_norm_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, clip, loss_scale);
+  return int(cudaGetLastError());
+}
+
+int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (grad_dtype == LAMB_GRAD_FP16)
+    moments_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, hp);
+  else
+    moments_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, hp);
+  return int(cudaGetLastError());
+}
+
+int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream) {
+  apply_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(T, hp);
+  return int(cudaGetLastError());
+}
+
+}  // namespace lambgb

@@ -1,0 +1,106 @@
+// Multi-tensor work table: lets thousands of ragged tensors go through one
+// launch per kernel.  Built once per handle on the host.
+//
+// Large tensors (more than kSmallMax elements) become chunk items of at most
+// kChunkElems elements, split evenly so the last chunk is not a sliver; chunk
+// starts are multiples of 8 elements so 128-bit loads stay aligned.  Small
+// tensors are packed whole, in tensor order, into pack items that one CTA
+// handles a warp per tensor, so a 1-element tensor does not cost a CTA.
+#include <algorithm>
+#include <cstring>
+#include <limits>
+
+#include "lamb_internal.h"
+
+namespace lambgb {
+
+bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string* err) {
+  plan->items.clear();
+  plan->pack_ids.clear();
+  plan->first_item.assign(size_t(std::max(n_tensors, 0)), -1);
+  plan->n_items.assign(size_t(std::max(n_tensors, 0)), 0);
+  if (n_tensors < 0) {
+    *err = "n_tensors must be >= 0";
+    return false;
+  }
+  if (n_tensors > 0 && !sizes) {
+    *err = "sizes is NULL";
+    return false;
+  }
+  const int64_t kMaxItems = std::numeric_limits<int32_t>::max();
+
+  int64_t pack_begin = 0, pack_elems = 0;
+  auto close_pack = [&]() {
+    const int64_t count = int64_t(plan->pack_ids.size()) - pack_begin;
+    if (count > 0) plan->items.push_back({pack_begin, int32_t(count), -1});
+    pack_begin = int64_t(plan->pack_ids.size());
+    pack_elems = 0;
+  };
+
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t n = sizes[i];
+    if (n < 0) {
+      *err = "sizes[" + std::to_string(i) + "] is negative";
+      return false;
+    }
+    if (n == 0) continue;
+    if (n <= kSmallMax) {
+      if (pack_elems + n > kPackBudget ||
+          int64_t(plan->pack_ids.size()) - pack_begin >= kPackMax) {
+        close_pack();
+      }
+      plan->pack_ids.push_back(i);
+      pack_elems += n;
+      continue;
+    }
+    const int64_t nchunks = (n + kChunkElems - 1) / kChunkElems;
+    int64_t per = (n + nchunks - 1) / nchunks;
+    per = (per + 7) / 8 * 8;
+    if (int64_t(plan->items.size()) + nchunks > kMaxItems) {
+      *err = "work table exceeds 2^31-1 items";
+      return false;
+    }
+    plan->first_item[size_t(i)] = int32_t(plan->items.size());
+    int32_t made = 0;
+    for (int64_t b = 0; b < n; b += per) {
+      plan->items.push_back({b, int32_t(std::min(per, n - b)), i});
+      ++made;
+    }
+    plan->n_items[size_t(i)] = made;
+  }
+  close_pack();
+  if (int64_t(plan->items.size()) > kMaxItems) {
+    *err = "work table exceeds 2^31-1 items";
+    return false;
+  }
+  return true;
+}
+
+}  // namespace lambgb
+
+extern "C" {
+
+LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, lamb_work_item* items,
+                       int64_t items_cap, int32_t* pack_ids, int64_t pack_cap, int64_t* n_items,
+                       int64_t* n_pack_ids) {
+  lambgb::Plan plan;
+  std::string err;
+  if (!lambgb::build_plan(n_tensors, sizes, &plan, &err)) return LAMB_ERR_INVALID;
+  const int64_t ni = int64_t(plan.items.size()), np = int64_t(plan.pack_ids.size());
+  if (n_items) *n_items = ni;
+  if (n_pack_ids) *n_pack_ids = np;
+  if ((items && items_cap < ni) || (pack_ids && pack_cap < np)) return LAMB_ERR_INVALID;
+  if (items && ni) std::memcpy(items, plan.items.data(), size_t(ni) * sizeof(lamb_work_item));
+  if (pack_ids && np) std::memcpy(pack_ids, plan.pack_ids.data(), size_t(np) * sizeof(int32_t));
+  return LAMB_OK;
+}
+
+LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* small_max, int64_t* pack_budget,
+                               int64_t* pack_max) {
+  if (chunk_elems) *chunk_elems = lambgb::kChunkElems;
+  if (small_max) *small_max = lambgb::kSmallMax;
+  if (pack_budget) *pack_budget = lambgb::kPackBudget;
+  if (pack_max) *pack_max = lambgb::kPackMax;
+}
+
+}  // extern "C"

@@ -1,0 +1,179 @@
+"""Python binding of the LAMB step library: marshalling of torch tensors to
+the C ABI of ``include/lamb.h``.  Every step of the optimizer runs in the
+library's CUDA kernels; PyTorch only owns the memory and the stream.
+
+LAMB (You et al., ICLR 2020) as adopted by MegaScale ("MegaScale: Scaling
+Large Language Model Training to More Than 10,000 GPUs", guided-reading
+digest, section 2), applied to one data-parallel rank's ZeRO-2 shard (digest
+section 3).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import LambError, LambHParams, LambResult, LambWorkItem, check
+
+_GRAD_CODES = {torch.bfloat16: _lib.LAMB_GRAD_BF16, torch.float16: _lib.LAMB_GRAD_FP16}
+
+
+def _ptrs(tensors) -> ctypes.Array:
+    arr = (ctypes.c_void_p * max(1, len(tensors)))()
+    for i, t in enumerate(tensors):
+        arr[i] = t.data_ptr() if t.numel() else None
+    return arr
+
+
+def _check_tensors(name, tensors, dtype, sizes, device):
+    if len(tensors) != len(sizes):
+        raise ValueError(f"{name}: expected {len(sizes)} tensors, got {len(tensors)}")
+    for i, (t, n) in enumerate(zip(tensors, sizes)):
+        if not isinstance(t, torch.Tensor) or t.dtype != dtype:
+            raise TypeError(f"{name}[{i}]: expected a {dtype} tensor")
+        if t.device != device:
+            raise ValueError(f"{name}[{i}]: on {t.device}, expected {device}")
+        if not t.is_contiguous() or t.numel() != n:
+            raise ValueError(f"{name}[{i}]: must be contiguous with {n} elements")
+
+
+class Lamb:
+    """LAMB optimizer state bound to caller-owned CUDA tensors.
+
+    ``weights``, ``exp_avg``, ``exp_avg_sq``: fp32 tensors updated in place;
+    ``weights_bf16``: bf16 tensors receiving the rounded weights; ``wd_flags``:
+    per-tensor 0/1 (1 = apply weight decay).  All tensors must be contiguous,
+    16-byte aligned and on one CUDA device.  ``stream`` defaults to the
+    current torch stream at construction; every step runs on it.
+    """
+
+    def __init__(self, weights: Sequence[torch.Tensor], exp_avg: Sequence[torch.Tensor],
+                 exp_avg_sq: Sequence[torch.Tensor], weights_bf16: Sequence[torch.Tensor],
+                 wd_flags: Sequence[int], *, beta1: float = 0.9, beta2: float = 0.999,
+                 eps: float = 1e-6, weight_decay: float = 0.01,
+                 grad_dtype: torch.dtype = torch.bfloat16, stream=None):
+        self._lib = _lib.load()
+        self._h = None
+        if grad_dtype not in _GRAD_CODES:
+            raise TypeError("grad_dtype must be torch.bfloat16 or torch.float16")
+        n = len(weights)
+        if len(wd_flags) != n:
+            raise ValueError("wd_flags must have one entry per tensor")
+        self.sizes = [int(t.numel()) for t in weights]
+        self.device = weights[0].device if n else torch.device("cuda", torch.cuda.current_device())
+        if self.device.type != "cuda":
+            raise ValueError("LAMB state must live on a CUDA device")
+        _check_tensors("weights", weights, torch.float32, self.sizes, self.device)
+        _check_tensors("exp_avg", exp_avg, torch.float32, self.sizes, self.device)
+        _check_tensors("exp_avg_sq", exp_avg_sq, torch.float32, self.sizes, self.device)
+        _check_tensors("weights_bf16", weights_bf16, torch.bfloat16, self.sizes, self.device)
+        self.grad_dtype = grad_dtype
+        self._keep = (list(weights), list(exp_avg), list(exp_avg_sq), list(weights_bf16))
+        with torch.cuda.device(self.device):
+            self.stream = stream if stream is not None else torch.cuda.current_stream()
+            hp = LambHParams(beta1, beta2, eps, weight_decay, _GRAD_CODES[grad_dtype])
+            sizes = np.asarray(self.sizes, dtype=np.int64)
+            flags = np.asarray([1 if f else 0 for f in wd_flags], dtype=np.uint8)
+            h = ctypes.c_void_p()
+            check(self._lib.lamb_create(
+                ctypes.byref(h), n, sizes.ctypes.data, flags.ctypes.data, _ptrs(weights),
+                _ptrs(exp_avg), _ptrs(exp_avg_sq), _ptrs(weights_bf16), ctypes.byref(hp),
+                ctypes.c_void_p(self.stream.cuda_stream)))
+        self._h = h
+        self._n = n
+        self._grad_ptrs = None
+        self._grads_keep = None
+        self._result = LambResult()
+
+    # ------------------------------------------------------------------ steps
+    def set_grads(self, grads: Sequence[torch.Tensor]) -> None:
+        """Validate and remember the grad tensors used by ``step()``."""
+        _check_tensors("grads", grads, self.grad_dtype, self.sizes, self.device)
+        self._grads_keep = list(grads)
+        self._grad_ptrs = _ptrs(grads)
+
+    def step(self, lr: float, t: int, clip: float = 0.0, loss_scale: float = 1.0,
+             grads: Sequence[torch.Tensor] | None = None):
+        """One LAMB step; returns ``(skipped, grad_norm)``.
+
+        ``grads`` (optional) replaces the tensors given to ``set_grads``.  The
+        call returns after the step has finished on the GPU.
+        """
+        if self._h is None:
+            raise RuntimeError("handle is closed")
+        if grads is not None:
+            self.set_grads(grads)
+        if self._grad_ptrs is None:
+            raise ValueError("no grads: pass grads= or call set_grads first")
+        check(self._lib.lamb_step(self._h, self._grad_ptrs, float(lr), int(t), float(clip),
+                                  float(loss_scale), ctypes.byref(self._result)))
+        return bool(self._result.skipped), float(self._result.grad_norm)
+
+    def trust(self) -> np.ndarray:
+        """Per-tensor trust ratios of the last step that was not skipped."""
+        out = np.empty(max(1, self._n), dtype=np.float32)
+        check(self._lib.lamb_get_trust(self._h, out.ctypes.data, self._n))
+        return out[: self._n]
+
+    def set_timing(self, enable: bool = True) -> None:
+        """Turn the library's CUDA event monitor on or off."""
+        check(self._lib.lamb_set_timing(self._h, 1 if enable else 0))
+
+    def kernel_times(self):
+        """Device milliseconds of the last step's (grad-norm, moments, apply) kernels."""
+        ms = (ctypes.c_float * 3)()
+        check(self._lib.lamb_kernel_times(self._h, ms))
+        return float(ms[0]), float(ms[1]), float(ms[2])
+
+    def close(self) -> None:
+        if self._h is not None:
+            h, self._h = self._h, None
+            check(self._lib.lamb_destroy(h))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+# --------------------------------------------------------------- work table
+def plan(sizes: Sequence[int]):
+    """The work table ``lamb_create`` would build for these sizes (host only).
+
+    Returns ``(items, pack_ids)``: a structured array with fields
+    ``begin, count, tensor`` and an int32 array of packed tensor ids.
+    """
+    lib = _lib.load()
+    s = np.ascontiguousarray(np.asarray(sizes, dtype=np.int64))
+    ni, npk = ctypes.c_int64(), ctypes.c_int64()
+    rc = lib.lamb_plan(len(s), s.ctypes.data, None, 0, None, 0, ctypes.byref(ni),
+                       ctypes.byref(npk))
+    check(rc)
+    items = (LambWorkItem * max(1, ni.value))()
+    packs = np.zeros(max(1, npk.value), dtype=np.int32)
+    check(lib.lamb_plan(len(s), s.ctypes.data, items, ni.value, packs.ctypes.data, npk.value,
+                        ctypes.byref(ni), ctypes.byref(npk)))
+    dt = np.dtype([("begin", np.int64), ("count", np.int32), ("tensor", np.int32)])
+    arr = np.frombuffer(bytes(items), dtype=dt)[: ni.value].copy()
+    return arr, packs[: npk.value].copy()
+
+
+def plan_limits() -> dict:
+    lib = _lib.load()
+    vals = [ctypes.c_int64() for _ in range(4)]
+    lib.lamb_plan_limits(*[ctypes.byref(v) for v in vals])
+    return dict(zip(("chunk_elems", "small_max", "pack_budget", "pack_max"),
+                    (v.value for v in vals)))
+
+
+__all__ = ["Lamb", "LambError", "plan", "plan_limits"]

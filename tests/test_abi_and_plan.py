@@ -1,0 +1,154 @@
+"""Host-side tests of the C ABI: the library builds and loads without a GPU,
+exports every symbol include/lamb.h declares, and builds a work table that
+covers every element of every tensor exactly once with aligned chunk starts."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import optimizer_step_gb300 as og
+from optimizer_step_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lamb.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"LAMB_API\s+[\w\s\*]+?\b(lamb_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_symbols() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = og.load()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", og.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(declared_symbols()) <= exported
+    # Nothing else of ours leaks out of the library.
+    assert not [s for s in exported if s.startswith("lamb") and s not in declared_symbols()]
+
+
+def check_plan(sizes):
+    lim = og.plan_limits()
+    items, packs = og.plan(sizes)
+    covered = [np.zeros(n, np.int32) if n <= 1 << 24 else None for n in sizes]
+    counts = {}
+    seen_packed = []
+    for it in items:
+        b, c, t = int(it["begin"]), int(it["count"]), int(it["tensor"])
+        assert c > 0
+        if t >= 0:
+            n = sizes[t]
+            assert n > lim["small_max"]
+            assert c <= lim["chunk_elems"] and b % 8 == 0 and b + c <= n
+            counts.setdefault(t, []).append((b, c))
+            if covered[t] is not None:
+                covered[t][b:b + c] += 1
+        else:
+            ids = packs[b:b + c]
+            assert c <= lim["pack_max"]
+            assert sum(sizes[i] for i in ids) <= lim["pack_budget"]
+            for i in ids:
+                assert 0 < sizes[i] <= lim["small_max"]
+                seen_packed.append(int(i))
+                if covered[i] is not None:
+                    covered[i][:] += 1
+    for t, segs in counts.items():
+        segs.sort()
+        at = 0
+        for b, c in segs:
+            assert b == at
+            at += c
+        assert at == sizes[t]
+    # chunk items of one tensor are contiguous in the table
+    tens = [int(t) for t in items["tensor"] if t >= 0]
+    first = {}
+    for k, t in enumerate(tens):
+        first.setdefault(t, k)
+        assert k - first[t] < len(counts[t])
+    assert sorted(seen_packed) == seen_packed
+    assert len(set(seen_packed)) == len(seen_packed)
+    for i, n in enumerate(sizes):
+        if covered[i] is not None and n:
+            assert np.all(covered[i] == 1), i
+        if n == 0:
+            assert i not in counts and i not in seen_packed
+    return items, packs
+
+
+@pytest.mark.parametrize("sizes", [
+    [], [0], [1], [7, 8, 9], [4095, 4096, 4097], [32768, 32769, 65535, 65536, 65537],
+    [0, 1, 0, 5000, 0], [3] * 1000, [4096] * 20, [2**31 + 5], [12288 * 36864, 12288, 12288],
+])
+def test_plan_covers_every_element_once(sizes):
+    check_plan(sizes)
+
+
+def test_plan_ragged_config():
+    import workloads
+    wl = workloads.ragged()
+    items, packs = check_plan(wl.sizes)
+    lim = og.plan_limits()
+    big = [n for n in wl.sizes if n > lim["small_max"]]
+    assert len(items) >= sum((n + lim["chunk_elems"] - 1) // lim["chunk_elems"] for n in big)
+    small = [n for n in wl.sizes if n <= lim["small_max"]]
+    assert len(packs) == len(small)
+
+
+def test_plan_chunks_are_balanced():
+    lim = og.plan_limits()
+    n = 3 * lim["chunk_elems"] + 9
+    items, _ = og.plan([n])
+    counts = sorted(int(c) for c in items["count"])
+    assert len(counts) == 4 and counts[-1] - counts[0] <= 8 * len(counts)
+
+
+def test_plan_rejects_negative_sizes():
+    with pytest.raises(og.LambError):
+        og.plan([4, -1])
+
+
+def test_create_rejects_bad_arguments_without_touching_the_gpu():
+    """Argument checks run before any CUDA call."""
+    import ctypes
+    lib = og.load()
+    h = ctypes.c_void_p()
+    hp = _lib.LambHParams(0.9, 0.999, 1e-6, 0.01, 0)
+    sizes = np.array([8], np.int64)
+    flags = np.array([1], np.uint8)
+    good = (ctypes.c_void_p * 1)(256)
+    odd = (ctypes.c_void_p * 1)(258)
+    null = (ctypes.c_void_p * 1)(None)
+    assert lib.lamb_create(ctypes.byref(h), -1, None, None, None, None, None, None,
+                           ctypes.byref(hp), None) == _lib.LAMB_ERR_INVALID
+    assert b"n_tensors" in lib.lamb_last_error()
+    assert lib.lamb_create(ctypes.byref(h), 1, sizes.ctypes.data, flags.ctypes.data, good, good,
+                           odd, good, ctypes.byref(hp), None) == _lib.LAMB_ERR_ALIGN
+    assert lib.lamb_create(ctypes.byref(h), 1, sizes.ctypes.data, flags.ctypes.data, good, null,
+                           good, good, ctypes.byref(hp), None) == _lib.LAMB_ERR_INVALID
+    for bad in (_lib.LambHParams(1.0, 0.999, 1e-6, 0.01, 0),
+                _lib.LambHParams(0.9, -0.1, 1e-6, 0.01, 0),
+                _lib.LambHParams(0.9, 0.999, -1.0, 0.01, 0),
+                _lib.LambHParams(0.9, 0.999, 1e-6, float("nan"), 0),
+                _lib.LambHParams(0.9, 0.999, 1e-6, 0.01, 5)):
+        assert lib.lamb_create(ctypes.byref(h), 1, sizes.ctypes.data, flags.ctypes.data, good,
+                               good, good, good, ctypes.byref(bad), None) == _lib.LAMB_ERR_INVALID
+    neg = np.array([-3], np.int64)
+    assert lib.lamb_create(ctypes.byref(h), 1, neg.ctypes.data, flags.ctypes.data, good, good,
+                           good, good, ctypes.byref(hp), None) == _lib.LAMB_ERR_INVALID
+
+
+def test_step_rejects_bad_arguments_without_touching_the_gpu():
+    import ctypes
+    lib = og.load()
+    res = _lib.LambResult()
+    assert lib.lamb_step(None, None, 1e-3, 1, 0.0, 1.0, ctypes.byref(res)) == _lib.LAMB_ERR_INVALID
+    assert lib.lamb_destroy(None) == _lib.LAMB_OK

@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded
+inputs (see tests/parity.py for the tolerances).  All of these need a GPU."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from optimizer_step_gb300 import Lamb, LambError
+
+from parity import assert_close, check_bf16_copy, f32, run_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def custom(sizes, *, wd=None, zero=(), grad_dtype=torch.bfloat16, t0=1, clip=0.0, S=1.0,
+           warm=True, seed=7, inject=None, kind="normal", sigma=1e-3):
+    return W.Workload("custom", "custom", list(sizes),
+                      list(wd) if wd is not None else [1 if n > 4096 else 0 for n in sizes],
+                      list(zero), grad_dtype, t0=t0, lr=1e-3, clip=clip, loss_scale=S,
+                      warm_state=warm, grad_kind=kind, grad_sigma=sigma, seed=seed,
+                      inject=dict(inject or {}))
+
+
+# -------------------------------------------------- small shapes, all paths
+SHAPES = {
+    "one": [1],
+    "odd_tails": [1, 2, 3, 5, 7, 8, 9, 15, 17, 31, 33],
+    "small_pack_edges": [4095, 4096, 4097, 1, 4096],
+    "chunk_edges": [32767, 32768, 32769, 65536 + 3],
+    "several_tiles_ragged_tail": [5 * 32768 + 1234, 300001],
+    "many_small": [int(x) for x in np.random.default_rng(3).integers(1, 300, 700)],
+    "empty_mixed": [0, 17, 0, 40000, 0],
+}
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float16])
+def test_small_shapes_one_and_ten_steps(name, grad_dtype):
+    S = 1024.0 if grad_dtype == torch.float16 else 1.0
+    wl = custom(SHAPES[name], grad_dtype=grad_dtype, S=S, zero=[0], t0=3, clip=0.05)
+    run_parity(wl, 10, check_steps=(1, 10))
+
+
+def test_first_step_from_zero_state_with_zero_weight_tensors():
+    wl = custom([1000, 50000, 3, 8, 70000], zero=[1, 2], warm=False, t0=1)
+    run_parity(wl, 1, check_steps=(1,))
+
+
+def test_clip_active_and_inactive():
+    for clip in (1e-3, 1e6):
+        run_parity(custom([9000, 123457], clip=clip, t0=20), 2, check_steps=(1, 2))
+
+
+def test_heavy_tailed_grads():
+    run_parity(custom([200000, 77, 4096], kind="student_t3", sigma=1e-4, clip=1.0, t0=500), 3,
+               check_steps=(1, 3))
+
+
+@pytest.mark.parametrize("grad_dtype,kind", [(torch.bfloat16, "inf"), (torch.bfloat16, "nan"),
+                                             (torch.float16, "inf"), (torch.float16, "nan")])
+def test_nonfinite_grad_skips_bit_exactly(grad_dtype, kind):
+    S = 65536.0 if grad_dtype == torch.float16 else 1.0
+    wl = custom([5, 40000, 300, 70001], grad_dtype=grad_dtype, S=S, inject={2: kind})
+    st = W.make_state(wl, "cuda")
+    gflat, gv = W.grad_buffer(wl, "cuda")
+    opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, grad_dtype=grad_dtype)
+    W.fill_grads(wl, 1, gflat)
+    assert opt.step(1e-3, 1, 0.0, S, grads=gv)[0] is False
+    before = [x.clone() for x in (st.w_flat, st.m_flat, st.v_flat, st.w16_flat)]
+    W.fill_grads(wl, 2, gflat)
+    sk, gn = opt.step(1e-3, 2, 1.0, S)
+    assert sk is True and gn == math.inf
+    for a, b in zip(before, (st.w_flat, st.m_flat, st.v_flat, st.w16_flat)):
+        assert torch.equal(a.view(torch.int8), b.view(torch.int8))
+    # The next clean step proceeds normally (no stale flag left on the device).
+    W.fill_grads(wl, 3, gflat)
+    assert opt.step(1e-3, 2, 0.0, S)[0] is False
+    opt.close()
+
+
+def test_deterministic_across_runs():
+    wl = custom([300001, 17, 5000, 123])
+    outs = []
+    for _ in range(2):
+        st = W.make_state(wl, "cuda")
+        _, gv = W.make_grads(wl, 1, "cuda")
+        with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags) as opt:
+            r = opt.step(1e-3, 5, 0.1, 1.0, grads=gv)
+            outs.append((r, st.w_flat.clone(), st.m_flat.clone(), opt.trust().copy()))
+    assert outs[0][0] == outs[1][0]
+    assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
+    assert np.array_equal(outs[0][3], outs[1][3])
+
+
+def test_empty_handle_and_errors():
+    with Lamb([], [], [], [], []) as opt:
+        assert opt.step(1e-3, 1, grads=[]) == (False, 0.0)
+    st = W.make_state(custom([64]), "cuda")
+    _, gv = W.make_grads(custom([64]), 1, "cuda")
+    with Lamb(st.w, st.m, st.v, st.w16, [1]) as opt:
+        with pytest.raises(LambError):
+            opt.step(1e-3, 0, grads=gv)
+        with pytest.raises(LambError):
+            opt.step(1e-3, 1, loss_scale=0.0, grads=gv)
+        with pytest.raises(TypeError):
+            opt.step(1e-3, 1, grads=[gv[0].float()])
+        raw = torch.zeros(80, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(LambError) as e:
+            opt.step(1e-3, 1, grads=[raw[1:65]])
+        assert e.value.code == -2
+    w = torch.zeros(80, device="cuda")
+    with pytest.raises(LambError) as e:
+        Lamb([w[1:65]], [w[:64]], [w[:64]], [torch.zeros(64, dtype=torch.bfloat16, device="cuda")],
+             [1])
+    assert e.value.code == -2
+
+
+# ------------------------------------------------------- the named configs
+def test_config_tiny_one_and_ten_steps():
+    log = run_parity(W.tiny(), 10, check_steps=(1, 10))
+    assert log["skipped"] == [0] * 10
+
+
+def test_config_fp16_twenty_steps_with_injected_overflow():
+    wl = W.fp16_24()
+    first_block = list(range(6))
+    site7, site15 = W.injection_site(wl, 7), W.injection_site(wl, 15)
+    subset = sorted(set(first_block + [site7[0], site15[0], len(wl.sizes) - 1]))
+    log = run_parity(wl, 20, check_steps=(1, 6, 7, 8, 10, 15, 16, 20), subset=subset)
+    want = [1 if k in (7, 15) else 0 for k in range(1, 21)]
+    assert log["skipped"] == want
+
+
+def test_config_ragged_full_step_then_ten_steps():
+    wl = W.ragged()
+    run_parity(wl, 1, check_steps=(1,))
+    rng = np.random.default_rng(0)
+    subset = sorted(set(wl.zero_w) | set(int(i) for i in rng.choice(len(wl.sizes), 150, False))
+                    | {int(np.argmax(wl.sizes))})
+    run_parity(wl, 10, check_steps=(1, 10), subset=subset)
+
+
+def _large_one_step(wl, tensors):
+    """One step of a large config; every tensor in ``tensors`` is checked in
+    full against the oracle, one at a time (pre-step copies kept on the GPU)."""
+    st = W.make_state(wl, "cuda")
+    gflat, gv = W.make_grads(wl, 1, "cuda")
+    pre = {i: (st.w[i].clone(), st.m[i].clone(), st.v[i].clone()) for i in tensors}
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, grad_dtype=wl.grad_dtype) as opt:
+        sk, gn = opt.step(wl.lr, wl.t0, wl.clip, wl.loss_scale, grads=gv)
+        trust = opt.trust()
+    assert sk is False
+    g_host = [W.as_bits(x) for x in gv]
+    for i in tensors:
+        mask = np.zeros(len(wl.sizes), np.uint8)
+        mask[i] = 1
+        n = len(wl.sizes)
+        w = [None] * n
+        m = [None] * n
+        v = [None] * n
+        w16 = [None] * n
+        w[i], m[i], v[i] = (W.as_f32(x).copy() for x in pre[i])
+        w16[i] = np.zeros(wl.sizes[i], np.uint16)
+        del pre[i]
+        osk, ogn, otr = oracle.lamb_step(
+            w, m, v, w16, g_host, wl.wd_flags, grad_dtype=oracle.GRAD_BF16,
+            beta1=f32(wl.beta1), beta2=f32(wl.beta2), eps=f32(wl.eps),
+            weight_decay=f32(wl.weight_decay), lr=f32(wl.lr), t=wl.t0, clip=f32(wl.clip),
+            loss_scale=f32(wl.loss_scale), update_mask=mask, want_trust=True)
+        assert osk == 0
+        assert_close(np.array([gn]), np.array([ogn]), 1e-5, "grad_norm")
+        assert_close(trust[i:i + 1], otr[i:i + 1], 1e-5, f"trust[{i}]")
+        w_gpu = W.as_f32(st.w[i])
+        assert_close(w_gpu, w[i], 1e-5, f"w[{i}]")
+        assert_close(W.as_f32(st.m[i]), m[i], 1e-5, f"m[{i}]")
+        assert_close(W.as_f32(st.v[i]), v[i], 1e-5, f"v[{i}]")
+        check_bf16_copy(W.as_bits(st.w16[i]), w_gpu, w16[i], f"w16[{i}]")
+        del w, m, v, w16, w_gpu
+
+
+def test_config_175b_shard_full_step():
+    wl = W.shard175b()
+    _large_one_step(wl, list(range(len(wl.sizes))))
+
+
+def test_config_175b_shard_ten_steps_subset():
+    wl = W.shard175b()
+    run_parity(wl, 10, check_steps=(1, 10), subset=[1, 4, 5])
+
+
+def test_config_7b_one_step_and_ten_steps_subset():
+    wl = W.llama7b()
+    n = len(wl.sizes)
+    _large_one_step(wl, [0, 1, 2, 3, 4, 5, 6, n - 1])
+    run_parity(wl, 10, check_steps=(1, 10), subset=[0, 2, 5, 6, n - 1])
