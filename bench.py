@@ -55,6 +55,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--config", default="shard175b",
                    help="workload: shard175b (default), tiny, ragged, 7b, fp16")
+    p.add_argument("--max-elems", type=int, default=0,
+                   help="cut every tensor to at most this many elements (small cases for "
+                        "profiling); 0 = the full workload")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -245,6 +248,8 @@ def run_ours(args, world, rank, local):
     init_dist(world, "nccl")
     device = torch.device("cuda", local)
     wl = W.CONFIGS[args.config]()
+    if args.max_elems > 0:
+        wl = W.scaled(wl, args.max_elems)
     N = wl.n_params
     st = W.make_state(wl, device)
     gflat, gv = W.make_grads(wl, 1, device)
@@ -330,7 +335,10 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.description, "name": wl.name, "n_params": N,
+            "config": {"workload": wl.description + (f", every tensor cut to at most "
+                                                     f"{args.max_elems:,} elements"
+                                                     if args.max_elems > 0 else ""),
+                       "name": wl.name, "n_params": N,
                        "tensors": len(wl.sizes), "grad_dtype": str(wl.grad_dtype).split(".")[-1],
                        "t0": wl.t0, "clip": wl.clip, "loss_scale": wl.loss_scale,
                        "parallelism": f"replicas x{world} (one shard per GPU, no collective)",

@@ -37,9 +37,27 @@
 namespace lambgb {
 namespace {
 
+// Launch shape.  The unroll factors are the 8-element vectors each thread has
+// in flight per loop trip; the min-blocks values cap registers so that many
+// CTAs stay resident per SM (bytes in flight, not instruction count, bound a
+// streaming kernel).  They can be overridden at build time for tuning sweeps.
+#ifndef LAMB_UNROLL_B
+#define LAMB_UNROLL_B 1
+#endif
+#ifndef LAMB_MINBLOCKS_B
+#define LAMB_MINBLOCKS_B 4
+#endif
+#ifndef LAMB_UNROLL_C
+#define LAMB_UNROLL_C 1
+#endif
+#ifndef LAMB_MINBLOCKS_C
+#define LAMB_MINBLOCKS_C 4
+#endif
+#ifndef LAMB_MINBLOCKS_A
+#define LAMB_MINBLOCKS_A 4
+#endif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 2;  // 8-element vectors in flight per thread per loop trip
 
 // ------------------------------------------------------------ memory access
 // Everything is streamed once per kernel and the step's footprint is far
@@ -67,10 +85,8 @@ __device__ __forceinline__ float2 decode2<LAMB_GRAD_BF16>(uint32_t x) {
 }
 template <>
 __device__ __forceinline__ float2 decode2<LAMB_GRAD_FP16>(uint32_t x) {
-  __half2 h;
-  static_assert(sizeof(h) == sizeof(x), "half2 size");
-  memcpy(&h, &x, sizeof x);
-  return __half22float2(h);
+  return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xFFFFu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16))));
 }
 template <int DT>
 __device__ __forceinline__ float decode1(uint16_t x) {
@@ -120,6 +136,11 @@ __device__ __forceinline__ double2 block_sum2(double a, double b, double2* red) 
 __device__ __forceinline__ float trust_of(double sum_w2, double sum_r2) {
   const double wn = sqrt(sum_w2), rn = sqrt(sum_r2);
   return (wn > 0.0 && rn > 0.0) ? float(wn / rn) : 1.0f;
+}
+
+// fp32 -> bf16 bit pattern, round to nearest even (CUDA's conversion).
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
 // ------------------------------------------------------ per-element math
@@ -176,7 +197,7 @@ __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int6
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads) grad_norm_kernel(DevTables T, float clip,
+__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(DevTables T, float clip,
                                                              double loss_scale) {
   __shared__ double red[kWarps];
   __shared__ int is_last;
@@ -243,6 +264,7 @@ __device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_
   g += begin;
   const float wd = d.wd;
   const int64_t nv = n >> 3;
+  constexpr int kUnroll = LAMB_UNROLL_B;
   for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kUnroll) * nthr) {
     uint4 gq[kUnroll];
     float mr[kUnroll][8], vr[kUnroll][8], wr[kUnroll][8];
@@ -297,7 +319,7 @@ __device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads) moments_kernel(DevTables T, Hyper hp) {
+__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(DevTables T, Hyper hp) {
   __shared__ double2 red[kWarps];
   __shared__ int is_last;
   const StepScalars* sc = T.sc;
@@ -361,6 +383,7 @@ __device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, 
   uint16_t* __restrict__ w16 = d.w16 + begin;
   const float wd = d.wd;
   const int64_t nv = n >> 3;
+  constexpr int kUnroll = LAMB_UNROLL_C;
   for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kUnroll) * nthr) {
     float mr[kUnroll][8], vr[kUnroll][8], wr[kUnroll][8];
 #pragma unroll
@@ -386,11 +409,8 @@ __device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, 
         }
         uint32_t packed[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __nv_bfloat162 b2 =
-              __floats2bfloat162_rn(wr[u][2 * j], wr[u][2 * j + 1]);  // .x low half
-          memcpy(&packed[j], &b2, sizeof(uint32_t));
-        }
+        for (int j = 0; j < 4; ++j)  // element 2j in the low half (lower address)
+          packed[j] = bf16_bits(wr[u][2 * j]) | (bf16_bits(wr[u][2 * j + 1]) << 16);
 #pragma unroll
         for (int h = 0; h < 2; ++h) st_f4(w + 8 * k + 4 * h, get4(wr[u], h));
         st_u4(w16 + 8 * k, make_uint4(packed[0], packed[1], packed[2], packed[3]));
@@ -401,12 +421,11 @@ __device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, 
     const float r = e.direction(m[j], v[j], w[j], wd);
     const float wn = __fmaf_rn(-step, r, w[j]);
     w[j] = wn;
-    const __nv_bfloat16 b = __float2bfloat16_rn(wn);
-    memcpy(&w16[j], &b, sizeof(uint16_t));
+    w16[j] = static_cast<uint16_t>(bf16_bits(wn));
   }
 }
 
-__global__ void __launch_bounds__(kThreads) apply_kernel(DevTables T, Hyper hp) {
+__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTables T, Hyper hp) {
   const StepScalars* sc = T.sc;
   if (sc->skip) return;
   const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, 0.0f};

@@ -4,8 +4,11 @@ oracle on the same seeded inputs and compare element by element.
 Tolerances: relative error <= 1e-5 after one step and <= 1e-4 after two or
 more steps, with an absolute floor of 1e-9, for w, m, v and the grad norm.
 Skip flags must match exactly.  The bf16 weight copy must be exactly the
-bf16 rounding (nearest, ties to even) of the GPU's own fp32 weights and lie
-within one bf16 ulp of the oracle's copy.  Hyperparameters cross the C ABI as
+bf16 rounding (nearest, ties to even) of the GPU's own fp32 weights, and may
+differ from the oracle's copy by at most one bf16 ulp plus the fp32 weight
+tolerance (rounding two fp32 values that differ within the weight tolerance
+can land on bf16 neighbours, and near zero the weight tolerance itself can
+exceed a bf16 ulp).  Hyperparameters cross the C ABI as
 fp32, so the oracle is given those same fp32 values (widened to fp64).
 """
 from __future__ import annotations
@@ -43,14 +46,23 @@ def assert_close(got: np.ndarray, want: np.ndarray, rtol: float, what: str) -> N
 
 
 def check_bf16_copy(w16_gpu: np.ndarray, w_gpu: np.ndarray, w16_oracle: np.ndarray,
-                    what: str) -> int:
+                    w_oracle: np.ndarray, rtol: float, what: str) -> int:
     """Returns the number of elements whose bf16 copy differs from the oracle's."""
-    assert np.array_equal(w16_gpu, oracle.bf16_rne(w_gpu)), f"{what}: w16 != bf16_rne(w)"
+    exact = oracle.bf16_rne(w_gpu)
+    if not np.array_equal(w16_gpu, exact):
+        i = int(np.flatnonzero(w16_gpu != exact)[0])
+        raise AssertionError(f"{what}: w16 != bf16_rne(w) at {i}: {w16_gpu[i]:#06x} vs "
+                             f"{exact[i]:#06x} (w {w_gpu[i]!r})")
     a = oracle.decode_grad(w16_gpu, oracle.GRAD_BF16)
     b = oracle.decode_grad(w16_oracle, oracle.GRAD_BF16)
     ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(a), np.abs(b)))[1] - 8)
-    far = np.abs(a - b) > ulp
-    assert not far.any(), f"{what}: bf16 copy more than 1 ulp from the oracle's"
+    wtol = np.maximum(FLOOR, rtol * np.abs(np.asarray(w_oracle, np.float64)))
+    far = np.abs(a - b) > ulp + wtol
+    if far.any():
+        i = int(np.flatnonzero(far)[0])
+        raise AssertionError(f"{what}: {int(far.sum())} bf16 copies too far from the oracle's; "
+                             f"first at {i}: {a[i]!r} vs {b[i]!r} (w {w_gpu[i]!r} vs "
+                             f"{w_oracle[i]!r})")
     return int(np.count_nonzero(w16_gpu != w16_oracle))
 
 
@@ -94,7 +106,8 @@ def compare_state(st: W.State, hs: HostState, rtol: float, tag: str, opt: Lamb =
         assert_close(w_gpu, hs.w[i], rtol, f"{tag} w[{i}]")
         assert_close(W.as_f32(st.m[i]), hs.m[i], rtol, f"{tag} m[{i}]")
         assert_close(W.as_f32(st.v[i]), hs.v[i], rtol, f"{tag} v[{i}]")
-        mism += check_bf16_copy(W.as_bits(st.w16[i]), w_gpu, hs.w16[i], f"{tag} w16[{i}]")
+        mism += check_bf16_copy(W.as_bits(st.w16[i]), w_gpu, hs.w16[i], hs.w[i], rtol,
+                                f"{tag} w16[{i}]")
         count += st.wl.sizes[i]
     if opt is not None and trust_oracle is not None:
         tg = opt.trust()

@@ -177,7 +177,7 @@ def _large_one_step(wl, tensors):
         assert_close(w_gpu, w[i], 1e-5, f"w[{i}]")
         assert_close(W.as_f32(st.m[i]), m[i], 1e-5, f"m[{i}]")
         assert_close(W.as_f32(st.v[i]), v[i], 1e-5, f"v[{i}]")
-        check_bf16_copy(W.as_bits(st.w16[i]), w_gpu, w16[i], f"w16[{i}]")
+        check_bf16_copy(W.as_bits(st.w16[i]), w_gpu, w16[i], w[i], 1e-5, f"w16[{i}]")
         del w, m, v, w16, w_gpu
 
 
