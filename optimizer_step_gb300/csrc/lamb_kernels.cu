@@ -45,13 +45,13 @@ namespace {
 #define LAMB_UNROLL_B 1
 #endif
 #ifndef LAMB_MINBLOCKS_B
-#define LAMB_MINBLOCKS_B 4
+#define LAMB_MINBLOCKS_B 3
 #endif
 #ifndef LAMB_UNROLL_C
 #define LAMB_UNROLL_C 1
 #endif
 #ifndef LAMB_MINBLOCKS_C
-#define LAMB_MINBLOCKS_C 4
+#define LAMB_MINBLOCKS_C 3
 #endif
 #ifndef LAMB_MINBLOCKS_A
 #define LAMB_MINBLOCKS_A 4
