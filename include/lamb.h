@@ -200,6 +200,48 @@ LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, lamb_work_item* 
 LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* small_max, int64_t* pack_budget,
                                int64_t* pack_max);
 
+/*
+ * Allocation-free grad-norm pass.  The pages have no counterpart of this
+ * entry point: it exists for callers that cannot allocate device memory when
+ * they need the check -- for example a framework whose caching allocator has
+ * already reserved nearly all of HBM, so that a raw cudaMalloc behind its back
+ * would fail or fragment its pool, or an out-of-memory recovery path that must
+ * look for inf/NaN grads exactly when no memory is left.
+ *
+ * It computes what lamb_step's first kernel computes, for grads the caller
+ * passes, without a handle:
+ *   out[0] = ||g / S|| over all tensors (+inf if any grad is inf or NaN)
+ *   out[1] = clip factor c = clip / out[0] if clip > 0 and out[0] > clip, else 1
+ *            (0 when a grad is not finite)
+ *   out[2] = 1.0 if any grad is inf or NaN, else 0.0
+ *
+ *   n_tensors   0 .. LAMB_NOALLOC_MAX_TENSORS; more is rejected with
+ *               LAMB_ERR_INVALID and a message naming the limit
+ *   sizes       host array of element counts (>= 0)
+ *   grads       host array of device pointers (grad_dtype elements, 16-byte
+ *               aligned; may be NULL for empty tensors)
+ *   out         device pointer to 3 doubles (8-byte aligned), written by the
+ *               kernel when the stream reaches it
+ *   stream      cudaStream_t the work is enqueued on (NULL: legacy default)
+ *
+ * It allocates nothing: no cudaMalloc, no cudaFree, no pinned memory.  Its
+ * scratch (tensor table, per-CTA partial sums, completion ticket) is one
+ * fixed device array of LAMB_NOALLOC_SCRATCH_BYTES inside this library, which
+ * every GPU that loads the library holds until the process exits.  The first
+ * call on each device looks up that array's device address and sizes the
+ * grid (with the device current); make that first call before any stream
+ * capture.  Every call reuses the same array and clears its ticket and flag
+ * first, so calls whose work overlaps on the GPU (on different streams or
+ * host threads without ordering between them) race and give wrong results;
+ * calls in one stream are ordered and safe.  The call returns once the work
+ * is enqueued.
+ */
+#define LAMB_NOALLOC_MAX_TENSORS 8192
+#define LAMB_NOALLOC_SCRATCH_BYTES (256 + 1024 * 8 + LAMB_NOALLOC_MAX_TENSORS * 16)
+LAMB_API int lamb_grad_norm_noalloc(int32_t n_tensors, const int64_t* sizes,
+                                    const void* const* grads, int32_t grad_dtype,
+                                    float loss_scale, float clip, double* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

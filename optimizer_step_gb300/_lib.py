@@ -22,7 +22,8 @@ LAMB_GRAD_FP16 = 1
 
 # Every symbol include/lamb.h declares.
 EXPORTS = ("lamb_create", "lamb_step", "lamb_destroy", "lamb_last_error", "lamb_get_trust",
-           "lamb_set_timing", "lamb_kernel_times", "lamb_plan", "lamb_plan_limits")
+           "lamb_set_timing", "lamb_kernel_times", "lamb_plan", "lamb_plan_limits",
+           "lamb_grad_norm_noalloc")
 
 
 class LambHParams(ctypes.Structure):
@@ -84,6 +85,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.lamb_plan.restype = ctypes.c_int
         lib.lamb_plan.argtypes = [i32, P, P, i64, P, i64, ctypes.POINTER(i64),
                                   ctypes.POINTER(i64)]
+        lib.lamb_grad_norm_noalloc.restype = ctypes.c_int
+        lib.lamb_grad_norm_noalloc.argtypes = [i32, P, P, i32, f32, f32, P, P]
         lib.lamb_plan_limits.restype = None
         lib.lamb_plan_limits.argtypes = [ctypes.POINTER(i64)] * 4
         _lib = lib

@@ -50,6 +50,8 @@ struct DeviceGuard {
 
 }  // namespace
 
+void lambgb::set_last_error(const std::string& msg) { g_last_error = msg; }
+
 struct lamb_handle {
   int device = 0;
   cudaStream_t stream = nullptr;

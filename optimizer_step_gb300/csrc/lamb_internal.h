@@ -75,6 +75,9 @@ struct Hyper {
   float eps, lr;
 };
 
+// Sets the calling thread's message returned by lamb_last_error().
+void set_last_error(const std::string& msg);
+
 // Kernel launchers (lamb_kernels.cu).  Each returns the launch's error code.
 int max_blocks_per_sm(int kernel, int grad_dtype);  // kernel: 0 norm, 1 moments, 2 apply
 int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip, double loss_scale,
