@@ -19,7 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblamb_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["lamb_kernels.cu", "lamb_api.cpp", "lamb_plan.cpp", "lamb_noalloc.cu"]
+SOURCES = ["lamb_kernels.cu", "lamb_api.cpp", "lamb_plan.cpp", "lamb_noalloc.cu",
+           "lamb_ptrs.cu"]
 HEADERS = [os.path.join(INCLUDE, "lamb.h"), os.path.join(CSRC, "lamb_internal.h")]
 
 

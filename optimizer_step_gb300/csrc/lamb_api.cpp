@@ -60,11 +60,11 @@ struct lamb_handle {
   Plan plan;
   std::vector<int64_t> sizes;
   void* dev_block = nullptr;       // every device table and scratch array
-  void* pinned = nullptr;          // grads staging + step scalars readback
-  const void** grads_stage = nullptr;
+  void* pinned = nullptr;          // step scalars readback
   StepScalars* scalars_host = nullptr;
-  std::vector<const void*> grads_cached;
-  bool grads_uploaded = false;
+  const void** grad_slot[kGradSlots] = {};        // device pointer arrays
+  std::vector<const void*> slot_ptrs[kGradSlots];  // what each slot holds (empty: unused)
+  int next_slot = 0;
   DevTables T{};
   int grid[3] = {0, 0, 0};
   bool timing = false;        // CUDA event monitor on
@@ -166,7 +166,8 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   const size_t o_td = carve(nt * sizeof(TensorDesc));
   const size_t o_items = carve(ni * sizeof(lamb_work_item));
   const size_t o_pack = carve(np * sizeof(int32_t));
-  const size_t o_grads = carve(nt * sizeof(void*));
+  size_t o_slot[kGradSlots];
+  for (auto& o : o_slot) o = carve(nt * sizeof(void*));
   const size_t o_g2 = carve(ni * sizeof(double));
   const size_t o_wr = carve(ni * sizeof(double2));
   const size_t o_ticket = carve(nt * sizeof(uint32_t));
@@ -177,21 +178,21 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
     delete h;
     return cuda_fail(ce, "cudaMalloc of the work table");
   }
-  ce = cudaMallocHost(&h->pinned, round_up(nt * sizeof(void*), 256) + sizeof(StepScalars));
+  ce = cudaMallocHost(&h->pinned, sizeof(StepScalars));
   if (ce != cudaSuccess) {
     cudaFree(h->dev_block);
     delete h;
     return cuda_fail(ce, "cudaMallocHost");
   }
   char* base = static_cast<char*>(h->dev_block);
-  h->grads_stage = static_cast<const void**>(h->pinned);
-  h->scalars_host = reinterpret_cast<StepScalars*>(static_cast<char*>(h->pinned) +
-                                                   round_up(nt * sizeof(void*), 256));
+  h->scalars_host = static_cast<StepScalars*>(h->pinned);
+  for (int k = 0; k < kGradSlots; ++k)
+    h->grad_slot[k] = reinterpret_cast<const void**>(base + o_slot[k]);
   DevTables& T = h->T;
   T.td = reinterpret_cast<const TensorDesc*>(base + o_td);
   T.items = reinterpret_cast<const lamb_work_item*>(base + o_items);
   T.pack_ids = reinterpret_cast<const int32_t*>(base + o_pack);
-  T.grads = reinterpret_cast<const void* const*>(base + o_grads);
+  T.grads = h->grad_slot[0];
   T.item_g2 = reinterpret_cast<double*>(base + o_g2);
   T.item_wr = reinterpret_cast<double2*>(base + o_wr);
   T.tensor_ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
@@ -265,17 +266,25 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   DeviceGuard dg(h->device);
   if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
   cudaError_t ce;
+  // Find this step's grad pointers among the device slots, or write them
+  // into the next slot.  No slot is in use: every earlier step waited for its
+  // stream before returning.
   const size_t nt = size_t(h->n_tensors);
-  if (!h->grads_uploaded ||
-      std::memcmp(h->grads_cached.data(), grads, nt * sizeof(void*)) != 0) {
-    // The staging area is free: every earlier step waited for its stream.
-    std::memcpy(h->grads_stage, grads, nt * sizeof(void*));
-    ce = cudaMemcpyAsync(const_cast<const void**>(h->T.grads), h->grads_stage,
-                         nt * sizeof(void*), cudaMemcpyHostToDevice, h->stream);
-    if (ce != cudaSuccess) return cuda_fail(ce, "uploading grad pointers");
-    h->grads_cached.assign(grads, grads + nt);
-    h->grads_uploaded = true;
+  int slot = -1;
+  for (int k = 0; k < kGradSlots && slot < 0; ++k) {
+    if (h->slot_ptrs[k].size() == nt &&
+        std::memcmp(h->slot_ptrs[k].data(), grads, nt * sizeof(void*)) == 0)
+      slot = k;
   }
+  if (slot < 0) {
+    slot = h->next_slot;
+    h->next_slot = (h->next_slot + 1) % kGradSlots;
+    h->slot_ptrs[slot].clear();
+    const int rc = write_grad_ptrs(h->grad_slot[slot], grads, h->n_tensors, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "writing grad pointers");
+    h->slot_ptrs[slot].assign(grads, grads + nt);
+  }
+  h->T.grads = h->grad_slot[slot];
 
   const double b1 = h->hp.beta1, b2 = h->hp.beta2;
   Hyper hy;

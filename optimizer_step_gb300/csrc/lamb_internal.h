@@ -85,4 +85,12 @@ int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip, d
 int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream);
 int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream);
 
+// Writes n grad pointers into the device array dst on the stream, by kernel
+// launches rather than a copy (lamb_ptrs.cu).  Returns the CUDA error code.
+int write_grad_ptrs(const void** dst, const void* const* src, int32_t n, void* stream);
+
+// Device grad-pointer arrays a handle keeps, so that alternating between a
+// few grad buffers (double buffering) needs no upload after the first use.
+constexpr int kGradSlots = 4;
+
 }  // namespace lambgb

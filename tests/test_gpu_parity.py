@@ -81,6 +81,28 @@ def test_nonfinite_grad_skips_bit_exactly(grad_dtype, kind):
     opt.close()
 
 
+def test_rotating_grad_buffers_match_the_oracle():
+    """Steps that take their grads from 5 different buffers in turn (more
+    buffers than the handle's grad-pointer slots) still match the oracle."""
+    from parity import HostState, compare_state, oracle_step
+    wl = custom([70001, 17, 5000, 40000], t0=4, clip=0.02)
+    st = W.make_state(wl, "cuda")
+    hs = HostState(st, None)
+    bufs = [W.grad_buffer(wl, "cuda") for _ in range(5)]
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags) as opt:
+        t = wl.t0
+        for k in range(1, 9):
+            flat, views = bufs[(k * 3) % 5]
+            W.fill_grads(wl, k, flat)
+            g_host = [W.as_bits(x) for x in views]
+            sk, gn = opt.step(wl.lr, t, wl.clip, wl.loss_scale, grads=views)
+            osk, ogn, otr = oracle_step(wl, hs, g_host, t)
+            assert not sk and not osk
+            assert_close(np.array([gn]), np.array([ogn]), 1e-4, f"step {k} grad_norm")
+            t += 1
+        compare_state(st, hs, 1e-4, "after 8 steps", opt, otr)
+
+
 def test_deterministic_across_runs():
     wl = custom([300001, 17, 5000, 123])
     outs = []
