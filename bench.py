@@ -39,8 +39,23 @@ METRIC = "LAMB step params/s and achieved HBM GB/s (% of GB300 peak), 175B-layer
 UNIT = "params/s"
 # Algorithmic HBM bytes per parameter of each kernel (16-bit grads, fp32 w/m/v,
 # bf16 weight copy): grad norm reads g; moments reads g, m, v, w and writes m, v;
-# apply reads m, v, w and writes w and the bf16 copy.
+# apply reads m, v, w and writes w and the bf16 copy.  Small tensors (packed,
+# at most small_max elements) are finished inside the moments kernel, which
+# then also writes their w and bf16 copy (28 B) while apply skips them.
 BYTES_PER_PARAM = {"grad_norm": 2, "moments": 22, "apply": 18}
+PACKED_BYTES_PER_PARAM = {"grad_norm": 2, "moments": 28, "apply": 0}
+
+
+def kernel_bytes(n_params: int, n_packed: int) -> dict:
+    """Algorithmic HBM bytes of one launch of each kernel."""
+    return {k: BYTES_PER_PARAM[k] * (n_params - n_packed) + PACKED_BYTES_PER_PARAM[k] * n_packed
+            for k in BYTES_PER_PARAM}
+
+
+def packed_params(sizes) -> int:
+    from optimizer_step_gb300 import plan_limits
+    small = plan_limits()["small_max"]
+    return int(sum(n for n in sizes if 0 < n <= small))
 FLOOR_BYTES_PER_PARAM = 28  # g read + w/m/v read and write + bf16 write
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -290,17 +305,20 @@ def run_ours(args, world, rank, local):
     sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
     value = whole_job_rate(N, args.steps, world, sec)
 
+    n_packed = packed_params(wl.sizes)
+    kbytes = kernel_bytes(N, n_packed)
+    step_bytes = sum(kbytes.values())
     kern = {}
     for j, name in enumerate(("grad_norm", "moments", "apply")):
         ms = statistics.mean(k[j] for k in ktimes)
-        gbs = BYTES_PER_PARAM[name] * N / (ms / 1e3) / 1e9
+        gbs = kbytes[name] / (ms / 1e3) / 1e9 if ms > 0 else 0.0
         kern[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
-                      "bytes_per_param": BYTES_PER_PARAM[name]}
+                      "bytes_per_launch": kbytes[name]}
     peak, peak_kind = hbm_peak()
     step_ms = sec / args.steps * 1e3
     dominant = "moments"
     achieved = kern[dominant]["GB/s"]
-    traffic = traffic_per_launch(dominant, N)
+    traffic = traffic_per_launch(dominant, N) if n_packed == 0 else None
 
     # ---- end to end: every step's grads come from pinned host memory.  Two
     # device grad buffers; the copy of step k+1 runs on a side stream while
@@ -363,13 +381,11 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "algorithmic_bytes": BYTES_PER_PARAM[dominant] * N},
+                         "algorithmic_bytes": kbytes[dominant]},
             "kernels": kern,
-            "step_hbm": {"bytes_per_param": sum(BYTES_PER_PARAM.values()),
-                         "GB/s": round(sum(BYTES_PER_PARAM.values()) * N / (step_ms / 1e3) / 1e9,
-                                       1),
-                         "frac_of_peak": round(sum(BYTES_PER_PARAM.values()) * N /
-                                               (step_ms / 1e3) / 1e9 / peak, 4),
+            "step_hbm": {"bytes_per_param": round(step_bytes / N, 4), "packed_params": n_packed,
+                         "GB/s": round(step_bytes / (step_ms / 1e3) / 1e9, 1),
+                         "frac_of_peak": round(step_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
                          "floor_28B_GB/s": round(FLOOR_BYTES_PER_PARAM * N / (step_ms / 1e3) /
                                                  1e9, 1)},
             "gpu_launches": 3 * args.steps,

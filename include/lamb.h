@@ -82,16 +82,40 @@ typedef struct {
 } lamb_hparams;
 
 /* Outcome of one step.
- *   skipped    1 if some grad was inf or NaN; the step then wrote nothing
- *              (w, m, v and w16 are bit-identical to before) and the caller
- *              should not advance t; 0 otherwise
- *   grad_norm  ||g / S|| over the whole shard, before clipping; +inf when
- *              skipped */
+ *   skipped          1 if some grad was inf or NaN; the step then wrote
+ *                    nothing (w, m, v and w16 are bit-identical to before) and
+ *                    the caller should not advance t; 0 otherwise
+ *   grad_norm        ||g / S|| over the whole shard, before clipping; +inf
+ *                    when skipped
+ *   loss_scale       the S this step divided the grads by
+ *   next_loss_scale  the S the next step will use: with a dynamic loss scaler
+ *                    (lamb_set_loss_scaler) the scale the next backward pass
+ *                    must multiply the loss by; otherwise equal to loss_scale */
 typedef struct {
   int32_t skipped;
   int32_t reserved;
   double grad_norm;
+  float loss_scale;
+  float next_loss_scale;
 } lamb_result;
+
+/* Dynamic loss scaling, kept on the GPU (see lamb_set_loss_scaler).
+ *   init_scale       S of the first step after enabling (finite, > 0)
+ *   growth_factor    S *= growth_factor after growth_interval clean steps in a
+ *                    row (>= 1; a product that is not finite is dropped)
+ *   backoff_factor   S *= backoff_factor after a skipped step (in (0, 1])
+ *   growth_interval  clean steps in a row before S grows (>= 1)
+ *   min_scale, max_scale  S never goes below min_scale after a backoff nor
+ *                    above max_scale after a growth (0 <= min <= init <= max;
+ *                    max may be +inf) */
+typedef struct {
+  float init_scale;
+  float growth_factor;
+  float backoff_factor;
+  int32_t growth_interval;
+  float min_scale;
+  float max_scale;
+} lamb_loss_scaler;
 
 /* One entry of the multi-tensor work table (see lamb_plan).
  *   tensor >= 0: elements [begin, begin + count) of that tensor;
@@ -135,17 +159,30 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
  *   lr          learning rate (finite)
  *   t           step number, >= 1 (bias corrections use b1^t and b2^t)
  *   clip        global grad-norm clip threshold; <= 0 disables clipping
- *   loss_scale  S > 0 (finite); grads are divided by S
+ *   loss_scale  S > 0 (finite); grads are divided by S (ignored while a
+ *               dynamic loss scaler is on)
  *   out         receives {skipped, grad_norm}
  *
  * Enqueues three kernels on the handle's stream (grad norm, moments and
- * per-tensor norms, apply), then copies the 24-byte outcome record to pinned host
- * memory and waits for it: the call returns when the step has finished on
- * the GPU.  The skip decision is taken on the GPU; the host never reads it in
+ * per-tensor norms, apply), then copies the small outcome record to pinned
+ * host memory and waits for it: the call returns when the step has finished
+ * on the GPU.  The skip decision is taken on the GPU; the host never reads it in
  * the middle of a step.
  */
 LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
                        float loss_scale, lamb_result* out);
+
+/*
+ * Turn dynamic loss scaling on (cfg non-NULL) or off (NULL).  While it is on,
+ * lamb_step ignores its loss_scale argument: the scale lives on the GPU, each
+ * step divides its grads by it, and the grad-norm kernel updates it right
+ * after deciding whether the step is skipped -- backoff after a skipped step,
+ * growth after growth_interval clean steps in a row -- with no host round
+ * trip.  lamb_result reports the scale a step used and the next one, which
+ * the next backward pass must use.  Enabling resets the scale to init_scale
+ * and the clean-step count to 0.  The scale is fp32, as at the interface.
+ */
+LAMB_API int lamb_set_loss_scaler(lamb_handle* h, const lamb_loss_scaler* cfg);
 
 /* Free everything the handle owns (after waiting for its stream).  NULL is a
  * no-op.  Caller-owned buffers are untouched. */
@@ -178,13 +215,19 @@ LAMB_API int lamb_set_timing(lamb_handle* h, int32_t enable);
 LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms);
 
 /*
- * Host-only view of the work table lamb_create builds (no GPU needed).
+ * Host-only view of a work table like the one lamb_create builds (no GPU
+ * needed).
  *
  * Tensors larger than small_max elements are split into chunks of at most
  * chunk_elems elements whose starts are multiples of 8 elements; tensors of
  * 1 .. small_max elements are packed whole, in order, into packs of at most
- * pack_budget elements and pack_max tensors; empty tensors get no work.
+ * max(chunk_elems, small_max) elements and pack_max tensors; empty tensors
+ * get no work.  Pack items come first, then each large tensor's chunks,
+ * contiguous and in tensor order.  lamb_create picks chunk_elems itself: the
+ * largest chunk (at most 32768) that still gives every resident CTA of the
+ * GPU about 8 items, and never below 2048.
  *
+ *   chunk_elems             0 (= 32768) or a multiple of 256 in [2048, 2^30]
  *   items, items_cap        output array for the work items (may be NULL)
  *   pack_ids, pack_cap      output array for packed tensor ids (may be NULL)
  *   n_items, n_pack_ids     receive the full counts
@@ -192,13 +235,14 @@ LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms);
  * Returns LAMB_ERR_INVALID (with the counts still set) when a capacity is too
  * small for a non-NULL output array.
  */
-LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, lamb_work_item* items,
-                       int64_t items_cap, int32_t* pack_ids, int64_t pack_cap, int64_t* n_items,
-                       int64_t* n_pack_ids);
+LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
+                       lamb_work_item* items, int64_t items_cap, int32_t* pack_ids,
+                       int64_t pack_cap, int64_t* n_items, int64_t* n_pack_ids);
 
-/* The constants lamb_plan uses (any output may be NULL). */
-LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* small_max, int64_t* pack_budget,
-                               int64_t* pack_max);
+/* The constants lamb_plan uses (any output may be NULL): the largest and the
+ * smallest chunk size, the largest packed tensor, and tensors per pack. */
+LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* min_chunk_elems,
+                               int64_t* small_max, int64_t* pack_max);
 
 /*
  * Allocation-free grad-norm pass.  The pages have no counterpart of this

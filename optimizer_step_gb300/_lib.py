@@ -23,7 +23,7 @@ LAMB_GRAD_FP16 = 1
 # Every symbol include/lamb.h declares.
 EXPORTS = ("lamb_create", "lamb_step", "lamb_destroy", "lamb_last_error", "lamb_get_trust",
            "lamb_set_timing", "lamb_kernel_times", "lamb_plan", "lamb_plan_limits",
-           "lamb_grad_norm_noalloc")
+           "lamb_set_loss_scaler", "lamb_grad_norm_noalloc")
 
 
 class LambHParams(ctypes.Structure):
@@ -33,7 +33,14 @@ class LambHParams(ctypes.Structure):
 
 class LambResult(ctypes.Structure):
     _fields_ = [("skipped", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("grad_norm", ctypes.c_double)]
+                ("grad_norm", ctypes.c_double), ("loss_scale", ctypes.c_float),
+                ("next_loss_scale", ctypes.c_float)]
+
+
+class LambLossScaler(ctypes.Structure):
+    _fields_ = [("init_scale", ctypes.c_float), ("growth_factor", ctypes.c_float),
+                ("backoff_factor", ctypes.c_float), ("growth_interval", ctypes.c_int32),
+                ("min_scale", ctypes.c_float), ("max_scale", ctypes.c_float)]
 
 
 class LambWorkItem(ctypes.Structure):
@@ -78,12 +85,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.lamb_last_error.argtypes = []
         lib.lamb_get_trust.restype = ctypes.c_int
         lib.lamb_get_trust.argtypes = [P, P, i32]
+        lib.lamb_set_loss_scaler.restype = ctypes.c_int
+        lib.lamb_set_loss_scaler.argtypes = [P, ctypes.POINTER(LambLossScaler)]
         lib.lamb_set_timing.restype = ctypes.c_int
         lib.lamb_set_timing.argtypes = [P, i32]
         lib.lamb_kernel_times.restype = ctypes.c_int
         lib.lamb_kernel_times.argtypes = [P, P]
         lib.lamb_plan.restype = ctypes.c_int
-        lib.lamb_plan.argtypes = [i32, P, P, i64, P, i64, ctypes.POINTER(i64),
+        lib.lamb_plan.argtypes = [i32, P, i64, P, i64, P, i64, ctypes.POINTER(i64),
                                   ctypes.POINTER(i64)]
         lib.lamb_grad_norm_noalloc.restype = ctypes.c_int
         lib.lamb_grad_norm_noalloc.argtypes = [i32, P, P, i32, f32, f32, P, P]

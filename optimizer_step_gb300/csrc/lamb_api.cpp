@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -67,6 +68,7 @@ struct lamb_handle {
   int next_slot = 0;
   DevTables T{};
   int grid[3] = {0, 0, 0};
+  ScaleArgs scaler{};         // dynamic == 1 while a dynamic loss scaler is on
   bool timing = false;        // CUDA event monitor on
   bool timed_step = false;    // a step has been timed since it was turned on
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -123,10 +125,26 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
                   "tensor " + std::to_string(i) + " has a pointer not 16-byte aligned");
   }
 
+  // Resident CTAs of the widest kernel, which set the work-table granularity.
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "querying the device");
+  int per_sm[3];
+  for (int k = 0; k < 3; ++k) {
+    per_sm[k] = max_blocks_per_sm(k, hp->grad_dtype);
+    if (per_sm[k] <= 0)
+      return cuda_fail(per_sm[k] < 0 ? cudaError_t(-per_sm[k]) : cudaErrorInvalidConfiguration,
+                       "occupancy query");
+  }
+  int64_t n_params = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) n_params += sizes[i];
+
   lamb_handle* h = new (std::nothrow) lamb_handle();
   if (!h) return fail(LAMB_ERR_NOMEM, "host allocation failed");
   std::string err;
-  if (!build_plan(n_tensors, sizes, &h->plan, &err)) {
+  const int64_t chunk = choose_chunk(n_params, int64_t(sms) * per_sm[1]);
+  if (!build_plan(n_tensors, sizes, chunk, &h->plan, &err)) {
     delete h;
     return fail(LAMB_ERR_INVALID, err);
   }
@@ -134,11 +152,7 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   h->hp = *hp;
   h->stream = static_cast<cudaStream_t>(stream);
   h->sizes.assign(sizes, sizes + n_tensors);
-  cudaError_t ce = cudaGetDevice(&h->device);
-  if (ce != cudaSuccess) {
-    delete h;
-    return cuda_fail(ce, "cudaGetDevice");
-  }
+  h->device = dev;
 
   // Host copies of the per-tensor records.
   const size_t nt = size_t(n_tensors), ni = h->plan.items.size(), np = h->plan.pack_ids.size();
@@ -173,6 +187,7 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   const size_t o_ticket = carve(nt * sizeof(uint32_t));
   const size_t o_trust = carve(nt * sizeof(float));
   const size_t o_sc = carve(sizeof(StepScalars));
+  const size_t o_queue = carve(2 * sizeof(uint32_t));
   ce = cudaMalloc(&h->dev_block, off);
   if (ce != cudaSuccess) {
     delete h;
@@ -198,6 +213,7 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   T.tensor_ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
   T.trust = reinterpret_cast<float*>(base + o_trust);
   T.sc = reinterpret_cast<StepScalars*>(base + o_sc);
+  T.queue = reinterpret_cast<uint32_t*>(base + o_queue);
   T.n_items = int32_t(ni);
 
   auto up = [&](size_t o, const void* src, size_t bytes) {
@@ -217,24 +233,8 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   }
 
   // Persistent grids: as many CTAs as fit at once, never more than the items.
-  int sms = 0;
-  ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
-  if (ce != cudaSuccess) {
-    cudaFreeHost(h->pinned);
-    cudaFree(h->dev_block);
-    delete h;
-    return cuda_fail(ce, "cudaDeviceGetAttribute");
-  }
   for (int k = 0; k < 3; ++k) {
-    int per_sm = max_blocks_per_sm(k, hp->grad_dtype);
-    if (per_sm <= 0) {
-      cudaFreeHost(h->pinned);
-      cudaFree(h->dev_block);
-      delete h;
-      return cuda_fail(per_sm < 0 ? cudaError_t(-per_sm) : cudaErrorInvalidConfiguration,
-                       "occupancy query");
-    }
-    const int64_t full = int64_t(per_sm) * sms;
+    const int64_t full = int64_t(per_sm[k]) * sms;
     h->grid[k] = int(std::max<int64_t>(1, std::min<int64_t>(full, int64_t(ni))));
   }
   *out = h;
@@ -261,7 +261,10 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   out->skipped = 0;
   out->reserved = 0;
   out->grad_norm = 0.0;
-  if (h->T.n_items == 0) return LAMB_OK;  // nothing to update: norm 0, no skip
+  out->loss_scale = loss_scale;
+  out->next_loss_scale = loss_scale;
+  // An empty shard still runs the (empty) kernels: the grad norm is 0 and a
+  // dynamic loss scale still advances.
 
   DeviceGuard dg(h->device);
   if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
@@ -298,8 +301,9 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   hy.lr = lr;
 
   if ((ce = mark(h, 0)) != cudaSuccess) return cuda_fail(ce, "event record");
-  int rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, clip, double(loss_scale),
-                            h->stream);
+  ScaleArgs sa = h->scaler;
+  sa.fixed = loss_scale;
+  int rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, clip, sa, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
   if ((ce = mark(h, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
   rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
@@ -315,7 +319,46 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the step");
   out->skipped = h->scalars_host->skip;
   out->grad_norm = h->scalars_host->grad_norm;
+  out->loss_scale = h->scalars_host->scale_used;
+  out->next_loss_scale = h->scaler.dynamic ? h->scalars_host->scale : loss_scale;
   if (h->timing) h->timed_step = true;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_set_loss_scaler(lamb_handle* h, const lamb_loss_scaler* cfg) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (!cfg) {
+    h->scaler = ScaleArgs{};
+    return LAMB_OK;
+  }
+  if (!(cfg->init_scale > 0.0f) || !std::isfinite(cfg->init_scale) ||
+      !(cfg->growth_factor >= 1.0f) || !std::isfinite(cfg->growth_factor) ||
+      !(cfg->backoff_factor > 0.0f && cfg->backoff_factor <= 1.0f) ||
+      cfg->growth_interval < 1 || !(cfg->min_scale >= 0.0f) ||
+      !(cfg->min_scale <= cfg->init_scale) || !(cfg->init_scale <= cfg->max_scale))
+    return fail(LAMB_ERR_INVALID,
+                "loss scaler: need init > 0 finite, growth >= 1, backoff in (0, 1], "
+                "interval >= 1, 0 <= min <= init <= max");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  // The scale and the clean-step count sit next to each other in StepScalars.
+  struct {
+    float scale;
+    int32_t good_steps;
+  } init{cfg->init_scale, 0};
+  static_assert(offsetof(StepScalars, good_steps) == offsetof(StepScalars, scale) + 4,
+                "scale and good_steps must be adjacent");
+  cudaError_t ce = cudaMemcpyAsync(reinterpret_cast<char*>(h->T.sc) + offsetof(StepScalars, scale),
+                                   &init, sizeof init, cudaMemcpyHostToDevice, h->stream);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(h->stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "initialising the loss scale");
+  h->scaler.dynamic = 1;
+  h->scaler.growth = cfg->growth_factor;
+  h->scaler.backoff = cfg->backoff_factor;
+  h->scaler.min_scale = cfg->min_scale;
+  h->scaler.max_scale = cfg->max_scale;
+  h->scaler.interval = cfg->growth_interval;
   return LAMB_OK;
 }
 

@@ -12,14 +12,21 @@
 
 namespace lambgb {
 
-// Work-table shape.  Large tensors are cut into chunks of at most kChunkElems
-// elements (multiples of 8, so every chunk start keeps 16-byte alignment of
-// the fp32 and 16-bit arrays); tensors up to kSmallMax elements are packed
-// whole, one warp per tensor, kPackBudget elements / kPackMax tensors a pack.
+// Work-table shape.  Large tensors are cut into chunks of at most
+// chunk_elems elements (a multiple of 256, so every chunk start keeps 16-byte
+// alignment of the fp32 and 16-bit arrays); tensors up to kSmallMax elements
+// are packed whole, one warp per tensor, at most max(chunk_elems, kSmallMax)
+// elements and kPackMax tensors a pack.  lamb_create picks chunk_elems from
+// the shard size and the GPU (choose_chunk), so that small shards still give
+// every resident CTA several items; kChunkElems is the largest value.
 constexpr int64_t kChunkElems = 32768;
+constexpr int64_t kMinChunkElems = 2048;
 constexpr int64_t kSmallMax = 4096;
-constexpr int64_t kPackBudget = 32768;
-constexpr int64_t kPackMax = 256;
+constexpr int64_t kPackMax = 64;
+constexpr int64_t kItemsPerSlot = 8;  // target work items per resident CTA
+
+// Chunk size for n_params elements on a GPU with cta_slots resident CTAs.
+int64_t choose_chunk(int64_t n_params, int64_t cta_slots);
 
 struct Plan {
   std::vector<lamb_work_item> items;
@@ -30,7 +37,8 @@ struct Plan {
 
 // Builds the work table; returns false (with a message) on invalid sizes or
 // a table too large for 32-bit item indices.
-bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string* err);
+bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems, Plan* plan,
+                std::string* err);
 
 // Per-tensor record the kernels read (device copy built at create time).
 struct TensorDesc {
@@ -53,6 +61,18 @@ struct StepScalars {
   int32_t skip;        // 1: a grad was inf/NaN, nothing is written
   uint32_t ticket;     // CTAs of the grad-norm kernel that have finished
   uint32_t nonfinite;  // OR of every CTA's inf/NaN flag
+  float scale_used;    // S of this step
+  float scale;         // dynamic loss scale for the next step
+  int32_t good_steps;  // clean steps in a row since the last growth/backoff
+  int32_t pad;
+};
+
+// How the grad-norm kernel finds this step's loss scale.
+struct ScaleArgs {
+  float fixed;          // S when dynamic == 0
+  int32_t dynamic;      // 1: S is StepScalars::scale, updated after the step
+  float growth, backoff, min_scale, max_scale;
+  int32_t interval;
 };
 
 // Device pointers of one handle, passed by value to every kernel.
@@ -61,11 +81,12 @@ struct DevTables {
   const int32_t* pack_ids;
   const TensorDesc* td;
   const void* const* grads;  // per-step grad pointers (device array)
-  double* item_g2;           // per work item: sum of raw g^2
+  double* item_g2;           // per CTA of the grad-norm kernel: sum of raw g^2
   double2* item_wr;          // per chunk item: (sum w^2, sum r^2)
   uint32_t* tensor_ticket;   // per tensor: chunk items finished this step
   float* trust;              // per tensor: trust ratio of this step
   StepScalars* sc;
+  uint32_t* queue;           // [2] item counters of the moments and apply kernels
   int32_t n_items;
 };
 
@@ -79,9 +100,11 @@ struct Hyper {
 void set_last_error(const std::string& msg);
 
 // Kernel launchers (lamb_kernels.cu).  Each returns the launch's error code.
-int max_blocks_per_sm(int kernel, int grad_dtype);  // kernel: 0 norm, 1 moments, 2 apply
-int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip, double loss_scale,
-                     void* stream);
+// max_blocks_per_sm: CTAs per SM a kernel's persistent grid uses (what fits,
+// capped per kernel); kernel 0 norm, 1 moments, 2 apply; negative: CUDA error.
+int max_blocks_per_sm(int kernel, int grad_dtype);
+int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip,
+                     const ScaleArgs& sa, void* stream);
 int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream);
 int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream);
 

@@ -10,15 +10,17 @@
 //
 // The exact method needs three passes, because r needs the global clip factor
 // and the update needs the whole tensor's ||r||:
-//   A  grad_norm_kernel  reads g (2 B/elem): sum of g^2, inf/NaN flag; its
-//      last CTA (atomic ticket, no waiting) forms ||g/S||, the clip factor and
-//      the skip flag on the device.
+//   A  grad_norm_kernel  reads g (2 B/elem): sum of g^2, inf/NaN flag, one
+//      partial per CTA; its last CTA (atomic ticket, no waiting) forms ||g/S||,
+//      the clip factor and the skip flag on the device.
 //   B  moments_kernel    reads g, m, v, w and writes m, v (22 B/elem); forms
 //      per-tensor sum w^2 and sum r^2; the last CTA of each tensor (ticket)
 //      turns them into trust_i.
 //   C  apply_kernel      reads m, v, w and writes w and the bf16 copy
 //      (18 B/elem); r is recomputed with the same function as in B, so the r
 //      applied is bit-identical to the r whose norm was taken.
+// Small tensors (packs) are finished inside B by the warp that owns them, so
+// they cost 30 B/elem instead of 42: the second pass over them hits cache.
 // Recomputing r costs the same bytes as storing it (B +4 B write, C reads r
 // instead of m and v), and avoids a 4 B/param scratch buffer.
 //
@@ -55,6 +57,23 @@ namespace {
 #endif
 #ifndef LAMB_MINBLOCKS_A
 #define LAMB_MINBLOCKS_A 4
+#endif
+// Resident CTAs per SM the persistent grids use (at most what fits): more
+// concurrent streams per SM than this measured slower on GB300.
+#ifndef LAMB_CTAS_PER_SM_A
+#define LAMB_CTAS_PER_SM_A 4
+#endif
+#ifndef LAMB_CTAS_PER_SM_B
+#define LAMB_CTAS_PER_SM_B 3
+#endif
+#ifndef LAMB_CTAS_PER_SM_C
+#define LAMB_CTAS_PER_SM_C 4
+#endif
+// 1: the moments and apply kernels take work items from an atomic counter
+// (greedy balance of ragged items); 0: static round-robin.  Results do not
+// depend on it: every partial is stored per item and summed in item order.
+#ifndef LAMB_DYNAMIC_BC
+#define LAMB_DYNAMIC_BC 1
 #endif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -169,23 +188,61 @@ __device__ __forceinline__ void put4(float (&a)[8], int h, float4 x) {
   a[4 * h + 3] = x.w;
 }
 
+// ------------------------------------------------------- item scheduling
+// Hands out work items to the CTAs of the moments and apply kernels: either
+// greedily from an atomic counter (reset by the grad-norm kernel's last CTA
+// before either kernel runs) or round-robin.  All threads of the CTA call
+// next() together; it returns the same item to all of them, or a value
+// >= n_items when the kernel's work is done.
+struct ItemQueue {
+  uint32_t* counter;
+  int32_t n_items;
+  int32_t* slot;  // shared memory
+  int32_t rr;
+  __device__ __forceinline__ int32_t next() {
+#if LAMB_DYNAMIC_BC
+    __syncthreads();  // everyone has read the previous item
+    if (threadIdx.x == 0) *slot = int32_t(atomicAdd(counter, 1u));
+    __syncthreads();
+    return *slot;
+#else
+    const int32_t it = rr;
+    rr += gridDim.x;
+    return it;
+#endif
+  }
+};
+
 // ===================================================== A: grad norm pass
 // Sum of raw g^2 and the inf/NaN flag over elements [0, n) of one grad array,
-// thread tid of nthr.
+// thread tid of nthr, added to the thread's fp64 total.  Each thread has up to
+// kLoadsA 16-byte loads in flight and sums at most 128 squares in fp32 before
+// folding them into fp64 (a chunk gives each thread at most 16 vectors; a
+// packed tensor of at most 4096 elements gives each lane at most 16).
+constexpr int kLoadsA = 4;
+
 template <int DT>
 __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int64_t n, int tid,
-                                            int nthr, float& acc, uint32_t& bad) {
+                                            int nthr, double& total, uint32_t& bad) {
   const int64_t nv = n >> 3;
-#pragma unroll 4
-  for (int64_t k = tid; k < nv; k += nthr) {
-    const uint4 q = ld_u4(g + 8 * k);
-    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+  float acc = 0.0f;
+  for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kLoadsA) * nthr) {
+    uint4 q[kLoadsA];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = decode2<DT>(wv[j]);
-      acc = __fmaf_rn(f.x, f.x, acc);
-      acc = __fmaf_rn(f.y, f.y, acc);
-      bad |= nonfinite2<DT>(wv[j]);
+    for (int u = 0; u < kLoadsA; ++u) {
+      const int64_t k = k0 + int64_t(u) * nthr;
+      q[u] = k < nv ? ld_u4(g + 8 * k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadsA; ++u) {
+      const uint32_t wv[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = decode2<DT>(wv[j]);
+        acc = __fmaf_rn(f.x, f.x, acc);
+        acc = __fmaf_rn(f.y, f.y, acc);
+        bad |= nonfinite2<DT>(wv[j]);
+      }
     }
   }
   for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {
@@ -194,36 +251,38 @@ __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int6
     acc = __fmaf_rn(f, f, acc);
     bad |= nonfinite2<DT>(uint32_t(x) | (uint32_t(x) << 16));
   }
+  total += double(acc);
 }
 
+// Each CTA walks its items (blockIdx.x, blockIdx.x + gridDim.x, ...) and
+// keeps one fp64 total per thread; one block reduction per CTA gives the
+// CTA's partial, and the CTA that finishes last (atomic ticket, nobody waits)
+// adds the gridDim.x partials in CTA order and publishes the step's scalars.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(DevTables T, float clip,
-                                                             double loss_scale) {
+                                                                               ScaleArgs sa) {
   __shared__ double red[kWarps];
   __shared__ int is_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t bad = 0;
+  double total = 0.0;
   for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
     const lamb_work_item wi = T.items[it];
-    float acc = 0.0f;
     if (wi.tensor >= 0) {
       const uint16_t* g = static_cast<const uint16_t*>(T.grads[wi.tensor]) + wi.begin;
-      sumsq_range<DT>(g, wi.count, threadIdx.x, kThreads, acc, bad);
+      sumsq_range<DT>(g, wi.count, threadIdx.x, kThreads, total, bad);
     } else {
       for (int k = warp; k < wi.count; k += kWarps) {
         const int32_t ti = T.pack_ids[wi.begin + k];
-        sumsq_range<DT>(static_cast<const uint16_t*>(T.grads[ti]), T.td[ti].n, lane, 32, acc,
+        sumsq_range<DT>(static_cast<const uint16_t*>(T.grads[ti]), T.td[ti].n, lane, 32, total,
                         bad);
       }
     }
-    const double s = block_sum(double(acc), red);
-    if (threadIdx.x == 0) T.item_g2[it] = s;
   }
-
-  // Completion ticket: the CTA that finishes last reduces every item's sum in
-  // item order and publishes the step's scalars.  Nobody waits.
+  const double cta_sum = block_sum(total, red);
   bad = __syncthreads_or(bad);
   if (threadIdx.x == 0) {
+    T.item_g2[blockIdx.x] = cta_sum;
     if (bad) atomicOr(&T.sc->nonfinite, 1u);
     __threadfence();
     const uint32_t prev = atomicAdd(&T.sc->ticket, 1u);
@@ -233,11 +292,13 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
   if (!is_last) return;
   __threadfence();
   double s = 0.0;
-  for (int32_t i = threadIdx.x; i < T.n_items; i += kThreads) s += __ldcg(&T.item_g2[i]);
+  for (int32_t i = threadIdx.x; i < int32_t(gridDim.x); i += kThreads) s += __ldcg(&T.item_g2[i]);
   s = block_sum(s, red);
   if (threadIdx.x == 0) {
     StepScalars* sc = T.sc;
     const uint32_t nf = atomicExch(&sc->nonfinite, 0u);
+    const float S = sa.dynamic ? sc->scale : sa.fixed;
+    const double loss_scale = double(S);
     if (nf) {
       sc->skip = 1;
       sc->grad_norm = __longlong_as_double(0x7FF0000000000000ll);  // +inf
@@ -249,7 +310,25 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
       sc->grad_norm = gn;
       sc->gscale = float(c / loss_scale);
     }
+    sc->scale_used = S;
+    if (sa.dynamic) {
+      // Loss scale for the next step: back off after an overflow, grow after
+      // `interval` clean steps in a row (fp32 products, clamped).
+      float next = S;
+      if (nf) {
+        next = __fmul_rn(S, sa.backoff);
+        if (next < sa.min_scale) next = sa.min_scale;
+        sc->good_steps = 0;
+      } else if (++sc->good_steps == sa.interval) {
+        const float grown = __fmul_rn(S, sa.growth);
+        if (isfinite(grown)) next = grown > sa.max_scale ? sa.max_scale : grown;
+        sc->good_steps = 0;
+      }
+      sc->scale = next;
+    }
     sc->ticket = 0u;  // ready for the next step
+    T.queue[0] = 0u;  // item counters of the moments and apply kernels
+    T.queue[1] = 0u;
   }
 }
 
@@ -318,63 +397,8 @@ __device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_
   }
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(DevTables T, Hyper hp) {
-  __shared__ double2 red[kWarps];
-  __shared__ int is_last;
-  const StepScalars* sc = T.sc;
-  if (sc->skip) return;
-  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, sc->gscale};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
-    const lamb_work_item wi = T.items[it];
-    if (wi.tensor >= 0) {
-      const TensorDesc d = T.td[wi.tensor];
-      float sw = 0.0f, sr = 0.0f;
-      moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[wi.tensor]), wi.begin, wi.count,
-                        threadIdx.x, kThreads, e, sw, sr);
-      const double2 s = block_sum2(sw, sr, red);
-      if (d.n_items == 1) {
-        if (threadIdx.x == 0) T.trust[wi.tensor] = trust_of(s.x, s.y);
-        continue;
-      }
-      if (threadIdx.x == 0) {
-        T.item_wr[it] = s;
-        __threadfence();
-        const uint32_t prev = atomicAdd(&T.tensor_ticket[wi.tensor], 1u);
-        is_last = prev == uint32_t(d.n_items - 1);
-      }
-      __syncthreads();
-      if (is_last) {
-        // Last chunk of this tensor: sum its chunks' partials in item order.
-        __threadfence();
-        double a = 0.0, b = 0.0;
-        for (int32_t k = threadIdx.x; k < d.n_items; k += kThreads) {
-          const double2 x = __ldcg(&T.item_wr[d.first_item + k]);
-          a += x.x;
-          b += x.y;
-        }
-        const double2 tot = block_sum2(a, b, red);
-        if (threadIdx.x == 0) {
-          T.trust[wi.tensor] = trust_of(tot.x, tot.y);
-          T.tensor_ticket[wi.tensor] = 0u;
-        }
-      }
-    } else {
-      for (int k = warp; k < wi.count; k += kWarps) {
-        const int32_t ti = T.pack_ids[wi.begin + k];
-        const TensorDesc d = T.td[ti];
-        float sw = 0.0f, sr = 0.0f;
-        moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[ti]), 0, d.n, lane, 32, e, sw,
-                          sr);
-        const double a = warp_sum(double(sw)), b = warp_sum(double(sr));
-        if (lane == 0) T.trust[ti] = trust_of(a, b);
-      }
-    }
-  }
-}
-
-// ========================================================= C: apply pass
+// Apply for elements [begin, begin + n) of one tensor (kernel C, and packed
+// tensors in kernel B): w <- w - step * r, then the bf16 copy.
 __device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, int64_t n, int tid,
                                             int nthr, const Elem& e, float step) {
   const float* __restrict__ m = d.m + begin;
@@ -425,24 +449,85 @@ __device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, 
   }
 }
 
+template <int DT>
+__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(DevTables T, Hyper hp) {
+  __shared__ double2 red[kWarps];
+  __shared__ int is_last;
+  const StepScalars* sc = T.sc;
+  if (sc->skip) return;
+  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, sc->gscale};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ int32_t slot;
+  ItemQueue q{&T.queue[0], T.n_items, &slot, int32_t(blockIdx.x)};
+  for (int32_t it = q.next(); it < T.n_items; it = q.next()) {
+    const lamb_work_item wi = T.items[it];
+    if (wi.tensor >= 0) {
+      const TensorDesc d = T.td[wi.tensor];
+      float sw = 0.0f, sr = 0.0f;
+      moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[wi.tensor]), wi.begin, wi.count,
+                        threadIdx.x, kThreads, e, sw, sr);
+      const double2 s = block_sum2(sw, sr, red);
+      if (d.n_items == 1) {
+        if (threadIdx.x == 0) T.trust[wi.tensor] = trust_of(s.x, s.y);
+        continue;
+      }
+      if (threadIdx.x == 0) {
+        T.item_wr[it] = s;
+        __threadfence();
+        const uint32_t prev = atomicAdd(&T.tensor_ticket[wi.tensor], 1u);
+        is_last = prev == uint32_t(d.n_items - 1);
+      }
+      __syncthreads();
+      if (is_last) {
+        // Last chunk of this tensor: sum its chunks' partials in item order.
+        __threadfence();
+        double a = 0.0, b = 0.0;
+#pragma unroll 8
+        for (int32_t k = threadIdx.x; k < d.n_items; k += kThreads) {
+          const double2 x = __ldcg(&T.item_wr[d.first_item + k]);
+          a += x.x;
+          b += x.y;
+        }
+        const double2 tot = block_sum2(a, b, red);
+        if (threadIdx.x == 0) {
+          T.trust[wi.tensor] = trust_of(tot.x, tot.y);
+          T.tensor_ticket[wi.tensor] = 0u;
+        }
+      }
+    } else {
+      // A packed small tensor belongs to one warp, which finishes it here:
+      // moments and norms, trust, then the update.  Each lane re-reads only
+      // the elements it has just written or read itself (same lane-to-element
+      // map in both passes), so the second pass hits cache, not HBM, and needs
+      // no synchronisation; the apply kernel skips pack items.
+      for (int k = warp; k < wi.count; k += kWarps) {
+        const int32_t ti = T.pack_ids[wi.begin + k];
+        const TensorDesc d = T.td[ti];
+        float sw = 0.0f, sr = 0.0f;
+        moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[ti]), 0, d.n, lane, 32, e, sw,
+                          sr);
+        const double a = warp_sum(double(sw)), b = warp_sum(double(sr));
+        const float tr = trust_of(a, b);
+        if (lane == 0) T.trust[ti] = tr;
+        apply_range(d, 0, d.n, lane, 32, e, __fmul_rn(hp.lr, tr));
+      }
+    }
+  }
+}
+
+// ========================================================= C: apply pass
 __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTables T, Hyper hp) {
   const StepScalars* sc = T.sc;
   if (sc->skip) return;
   const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, 0.0f};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
+  __shared__ int32_t slot;
+  ItemQueue q{&T.queue[1], T.n_items, &slot, int32_t(blockIdx.x)};
+  for (int32_t it = q.next(); it < T.n_items; it = q.next()) {
     const lamb_work_item wi = T.items[it];
-    if (wi.tensor >= 0) {
-      const TensorDesc d = T.td[wi.tensor];
-      const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
-      apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
-    } else {
-      for (int k = warp; k < wi.count; k += kWarps) {
-        const int32_t ti = T.pack_ids[wi.begin + k];
-        const TensorDesc d = T.td[ti];
-        apply_range(d, 0, d.n, lane, 32, e, __fmul_rn(hp.lr, T.trust[ti]));
-      }
-    }
+    if (wi.tensor < 0) continue;  // packs were finished by the moments kernel
+    const TensorDesc d = T.td[wi.tensor];
+    const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
+    apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
   }
 }
 
@@ -466,16 +551,19 @@ int max_blocks_per_sm(int kernel, int grad_dtype) {
   } else {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, apply_kernel, kThreads, 0);
   }
-  return err == cudaSuccess ? nb : -int(err);
+  if (err != cudaSuccess) return -int(err);
+  const int cap = kernel == 0 ? LAMB_CTAS_PER_SM_A : kernel == 1 ? LAMB_CTAS_PER_SM_B
+                                                                 : LAMB_CTAS_PER_SM_C;
+  return nb < cap ? nb : cap;
 }
 
-int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip, double loss_scale,
-                     void* stream) {
+int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip,
+                     const ScaleArgs& sa, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (grad_dtype == LAMB_GRAD_FP16)
-    grad_norm_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, clip, loss_scale);
+    grad_norm_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, clip, sa);
   else
-    grad_norm_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, clip, loss_scale);
+    grad_norm_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, clip, sa);
   return int(cudaGetLastError());
 }
 

@@ -2,10 +2,12 @@
 // launch per kernel.  Built once per handle on the host.
 //
 // Large tensors (more than kSmallMax elements) become chunk items of at most
-// kChunkElems elements, split evenly so the last chunk is not a sliver; chunk
+// chunk_elems elements, split evenly so the last chunk is not a sliver; chunk
 // starts are multiples of 8 elements so 128-bit loads stay aligned.  Small
 // tensors are packed whole, in tensor order, into pack items that one CTA
-// handles a warp per tensor, so a 1-element tensor does not cost a CTA.
+// handles a warp per tensor, so a 1-element tensor does not cost a CTA.  Pack
+// items come first in the table: their latency-bound work then overlaps the
+// first wave of chunk work instead of trailing at the end of a kernel.
 #include <algorithm>
 #include <cstring>
 #include <limits>
@@ -14,7 +16,15 @@
 
 namespace lambgb {
 
-bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string* err) {
+int64_t choose_chunk(int64_t n_params, int64_t cta_slots) {
+  const int64_t target = std::max<int64_t>(1, cta_slots) * kItemsPerSlot;
+  int64_t c = (n_params + target - 1) / target;
+  c = (c + kMinChunkElems - 1) / kMinChunkElems * kMinChunkElems;
+  return std::min(kChunkElems, std::max(kMinChunkElems, c));
+}
+
+bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems, Plan* plan,
+                std::string* err) {
   plan->items.clear();
   plan->pack_ids.clear();
   plan->first_item.assign(size_t(std::max(n_tensors, 0)), -1);
@@ -27,8 +37,14 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string
     *err = "sizes is NULL";
     return false;
   }
+  if (chunk_elems < kMinChunkElems || chunk_elems > (int64_t(1) << 30) || chunk_elems % 256) {
+    *err = "chunk_elems must be a multiple of 256 in [2048, 2^30]";
+    return false;
+  }
+  const int64_t pack_budget = std::max(chunk_elems, kSmallMax);
   const int64_t kMaxItems = std::numeric_limits<int32_t>::max();
 
+  // Packs of small tensors first, in tensor order.
   int64_t pack_begin = 0, pack_elems = 0;
   auto close_pack = [&]() {
     const int64_t count = int64_t(plan->pack_ids.size()) - pack_begin;
@@ -36,24 +52,25 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string
     pack_begin = int64_t(plan->pack_ids.size());
     pack_elems = 0;
   };
-
   for (int32_t i = 0; i < n_tensors; ++i) {
     const int64_t n = sizes[i];
     if (n < 0) {
       *err = "sizes[" + std::to_string(i) + "] is negative";
       return false;
     }
-    if (n == 0) continue;
-    if (n <= kSmallMax) {
-      if (pack_elems + n > kPackBudget ||
-          int64_t(plan->pack_ids.size()) - pack_begin >= kPackMax) {
-        close_pack();
-      }
-      plan->pack_ids.push_back(i);
-      pack_elems += n;
-      continue;
-    }
-    const int64_t nchunks = (n + kChunkElems - 1) / kChunkElems;
+    if (n == 0 || n > kSmallMax) continue;
+    if (pack_elems + n > pack_budget || int64_t(plan->pack_ids.size()) - pack_begin >= kPackMax)
+      close_pack();
+    plan->pack_ids.push_back(i);
+    pack_elems += n;
+  }
+  close_pack();
+
+  // Then the chunks of every large tensor, each tensor's chunks contiguous.
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t n = sizes[i];
+    if (n <= kSmallMax) continue;
+    const int64_t nchunks = (n + chunk_elems - 1) / chunk_elems;
     int64_t per = (n + nchunks - 1) / nchunks;
     per = (per + 7) / 8 * 8;
     if (int64_t(plan->items.size()) + nchunks > kMaxItems) {
@@ -68,7 +85,6 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string
     }
     plan->n_items[size_t(i)] = made;
   }
-  close_pack();
   if (int64_t(plan->items.size()) > kMaxItems) {
     *err = "work table exceeds 2^31-1 items";
     return false;
@@ -80,26 +96,33 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, Plan* plan, std::string
 
 extern "C" {
 
-LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, lamb_work_item* items,
-                       int64_t items_cap, int32_t* pack_ids, int64_t pack_cap, int64_t* n_items,
-                       int64_t* n_pack_ids) {
+LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
+                       lamb_work_item* items, int64_t items_cap, int32_t* pack_ids,
+                       int64_t pack_cap, int64_t* n_items, int64_t* n_pack_ids) {
   lambgb::Plan plan;
   std::string err;
-  if (!lambgb::build_plan(n_tensors, sizes, &plan, &err)) return LAMB_ERR_INVALID;
+  if (chunk_elems == 0) chunk_elems = lambgb::kChunkElems;
+  if (!lambgb::build_plan(n_tensors, sizes, chunk_elems, &plan, &err)) {
+    lambgb::set_last_error(err);
+    return LAMB_ERR_INVALID;
+  }
   const int64_t ni = int64_t(plan.items.size()), np = int64_t(plan.pack_ids.size());
   if (n_items) *n_items = ni;
   if (n_pack_ids) *n_pack_ids = np;
-  if ((items && items_cap < ni) || (pack_ids && pack_cap < np)) return LAMB_ERR_INVALID;
+  if ((items && items_cap < ni) || (pack_ids && pack_cap < np)) {
+    lambgb::set_last_error("output capacity too small");
+    return LAMB_ERR_INVALID;
+  }
   if (items && ni) std::memcpy(items, plan.items.data(), size_t(ni) * sizeof(lamb_work_item));
   if (pack_ids && np) std::memcpy(pack_ids, plan.pack_ids.data(), size_t(np) * sizeof(int32_t));
   return LAMB_OK;
 }
 
-LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* small_max, int64_t* pack_budget,
-                               int64_t* pack_max) {
+LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* min_chunk_elems,
+                               int64_t* small_max, int64_t* pack_max) {
   if (chunk_elems) *chunk_elems = lambgb::kChunkElems;
+  if (min_chunk_elems) *min_chunk_elems = lambgb::kMinChunkElems;
   if (small_max) *small_max = lambgb::kSmallMax;
-  if (pack_budget) *pack_budget = lambgb::kPackBudget;
   if (pack_max) *pack_max = lambgb::kPackMax;
 }
 

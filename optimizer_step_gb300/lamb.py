@@ -16,7 +16,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import LambError, LambHParams, LambResult, LambWorkItem, check
+from ._lib import LambError, LambHParams, LambLossScaler, LambResult, LambWorkItem, check
 
 _GRAD_CODES = {torch.bfloat16: _lib.LAMB_GRAD_BF16, torch.float16: _lib.LAMB_GRAD_FP16}
 
@@ -87,6 +87,8 @@ class Lamb:
         self._grad_ptrs = None
         self._grads_keep = None
         self._result = LambResult()
+        self.loss_scale = None       # S the last step used
+        self.next_loss_scale = None  # S the next step uses (dynamic scaling: for the backward)
 
     # ------------------------------------------------------------------ steps
     def set_grads(self, grads: Sequence[torch.Tensor]) -> None:
@@ -110,7 +112,25 @@ class Lamb:
             raise ValueError("no grads: pass grads= or call set_grads first")
         check(self._lib.lamb_step(self._h, self._grad_ptrs, float(lr), int(t), float(clip),
                                   float(loss_scale), ctypes.byref(self._result)))
+        self.loss_scale = float(self._result.loss_scale)
+        self.next_loss_scale = float(self._result.next_loss_scale)
         return bool(self._result.skipped), float(self._result.grad_norm)
+
+    def set_loss_scaler(self, init_scale: float = 65536.0, growth_factor: float = 2.0,
+                        backoff_factor: float = 0.5, growth_interval: int = 2000,
+                        min_scale: float = 1.0, max_scale: float = float("inf")) -> None:
+        """Keep the loss scale on the GPU and adapt it after every step (back off
+        after an overflow, grow after ``growth_interval`` clean steps); while on,
+        ``step``'s ``loss_scale`` argument is ignored and ``next_loss_scale``
+        tells the next backward pass which scale to use."""
+        cfg = LambLossScaler(init_scale, growth_factor, backoff_factor, int(growth_interval),
+                             min_scale, max_scale)
+        check(self._lib.lamb_set_loss_scaler(self._h, ctypes.byref(cfg)))
+        self.next_loss_scale = float(init_scale)
+
+    def clear_loss_scaler(self) -> None:
+        """Back to the fixed loss scale passed to each ``step``."""
+        check(self._lib.lamb_set_loss_scaler(self._h, None))
 
     def trust(self) -> np.ndarray:
         """Per-tensor trust ratios of the last step that was not skipped."""
@@ -147,22 +167,22 @@ class Lamb:
 
 
 # --------------------------------------------------------------- work table
-def plan(sizes: Sequence[int]):
-    """The work table ``lamb_create`` would build for these sizes (host only).
+def plan(sizes: Sequence[int], chunk_elems: int = 0):
+    """A work table like the one ``lamb_create`` builds (host only).
 
-    Returns ``(items, pack_ids)``: a structured array with fields
-    ``begin, count, tensor`` and an int32 array of packed tensor ids.
+    ``chunk_elems`` 0 means the largest chunk size.  Returns ``(items,
+    pack_ids)``: a structured array with fields ``begin, count, tensor`` and
+    an int32 array of packed tensor ids.
     """
     lib = _lib.load()
     s = np.ascontiguousarray(np.asarray(sizes, dtype=np.int64))
     ni, npk = ctypes.c_int64(), ctypes.c_int64()
-    rc = lib.lamb_plan(len(s), s.ctypes.data, None, 0, None, 0, ctypes.byref(ni),
-                       ctypes.byref(npk))
-    check(rc)
+    check(lib.lamb_plan(len(s), s.ctypes.data, int(chunk_elems), None, 0, None, 0,
+                        ctypes.byref(ni), ctypes.byref(npk)))
     items = (LambWorkItem * max(1, ni.value))()
     packs = np.zeros(max(1, npk.value), dtype=np.int32)
-    check(lib.lamb_plan(len(s), s.ctypes.data, items, ni.value, packs.ctypes.data, npk.value,
-                        ctypes.byref(ni), ctypes.byref(npk)))
+    check(lib.lamb_plan(len(s), s.ctypes.data, int(chunk_elems), items, ni.value,
+                        packs.ctypes.data, npk.value, ctypes.byref(ni), ctypes.byref(npk)))
     dt = np.dtype([("begin", np.int64), ("count", np.int32), ("tensor", np.int32)])
     arr = np.frombuffer(bytes(items), dtype=dt)[: ni.value].copy()
     return arr, packs[: npk.value].copy()
@@ -172,7 +192,7 @@ def plan_limits() -> dict:
     lib = _lib.load()
     vals = [ctypes.c_int64() for _ in range(4)]
     lib.lamb_plan_limits(*[ctypes.byref(v) for v in vals])
-    return dict(zip(("chunk_elems", "small_max", "pack_budget", "pack_max"),
+    return dict(zip(("chunk_elems", "min_chunk_elems", "small_max", "pack_max"),
                     (v.value for v in vals)))
 
 

@@ -58,6 +58,10 @@ def _load():
                 P, ctypes.c_int32, P, P, P]
             lib.oracle_decode_grad_n.restype = None
             lib.oracle_decode_grad_n.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P]
+            lib.oracle_loss_scale_update.restype = None
+            lib.oracle_loss_scale_update.argtypes = [
+                P, P, ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.c_int32,
+                ctypes.c_float, ctypes.c_float]
             lib.oracle_bf16_rne_n.restype = None
             lib.oracle_bf16_rne_n.argtypes = [P, ctypes.c_int64, P]
             _lib = lib
@@ -122,6 +126,17 @@ def lamb_step(w, m, v, w16, g, wd_flags, *, grad_dtype, beta1, beta2, eps, weigh
     if want_trust:
         return int(skipped.value), float(gn.value), trust
     return int(skipped.value), float(gn.value)
+
+
+def loss_scale_update(scale, good_steps, found_inf, *, growth=2.0, backoff=0.5,
+                      growth_interval=2000, min_scale=0.0, max_scale=float("inf")):
+    """One dynamic loss-scale update; returns the new (scale, good_steps)."""
+    s = ctypes.c_float(scale)
+    g = ctypes.c_int32(good_steps)
+    _load().oracle_loss_scale_update(ctypes.addressof(s), ctypes.addressof(g),
+                                     1 if found_inf else 0, growth, backoff,
+                                     growth_interval, min_scale, max_scale)
+    return float(s.value), int(g.value)
 
 
 def decode_grad(bits: np.ndarray, grad_dtype: int) -> np.ndarray:

@@ -172,6 +172,25 @@ void oracle_bf16_rne_n(const float* x, int64_t n, uint16_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = bf16_rne(x[i]);
 }
 
+void oracle_loss_scale_update(float* scale, int32_t* good_steps, int32_t found_inf,
+                              float growth, float backoff, int32_t growth_interval,
+                              float min_scale, float max_scale) {
+  float s = *scale;
+  if (found_inf) {
+    s = s * backoff;
+    if (s < min_scale) s = min_scale;
+    *good_steps = 0;
+  } else {
+    *good_steps += 1;
+    if (*good_steps == growth_interval) {
+      const float grown = s * growth;
+      if (std::isfinite(grown)) s = grown > max_scale ? max_scale : grown;
+      *good_steps = 0;
+    }
+  }
+  *scale = s;
+}
+
 int oracle_lamb_step(int32_t n_tensors, const int64_t* sizes, const uint8_t* wd_flags,
                      float* const* w, float* const* m, float* const* v, uint16_t* const* w16,
                      const uint16_t* const* g, int32_t grad_dtype, double beta1, double beta2,

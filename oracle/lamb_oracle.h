@@ -83,6 +83,19 @@ int oracle_lamb_step(int32_t n_tensors, const int64_t* sizes, const uint8_t* wd_
                      const uint8_t* update_mask, int32_t n_threads,
                      int32_t* skipped, double* grad_norm, double* trust_out);
 
+/*
+ * Dynamic loss scaling between steps (the scale is fp32, as the loss scale
+ * crosses the library's interface as fp32).  After a step that saw an inf or
+ * NaN grad: scale *= backoff, clamped below at min_scale, and the count of
+ * clean steps restarts.  After a clean step: the count grows by one, and when
+ * it reaches growth_interval the scale is multiplied by growth (kept only if
+ * the product is finite, clamped above at max_scale) and the count restarts.
+ * Updates *scale and *good_steps in place.
+ */
+void oracle_loss_scale_update(float* scale, int32_t* good_steps, int32_t found_inf,
+                              float growth, float backoff, int32_t growth_interval,
+                              float min_scale, float max_scale);
+
 /* Decode one bf16 / fp16 bit pattern to double (IEEE 754 binary16 and the
  * top half of binary32, written out from their definitions). */
 double oracle_decode_grad(uint16_t bits, int32_t grad_dtype);

@@ -36,26 +36,31 @@ def test_library_exports_every_declared_symbol():
     assert not [s for s in exported if s.startswith("lamb") and s not in declared_symbols()]
 
 
-def check_plan(sizes):
+def check_plan(sizes, chunk=0):
     lim = og.plan_limits()
-    items, packs = og.plan(sizes)
+    chunk_elems = chunk or lim["chunk_elems"]
+    pack_budget = max(chunk_elems, lim["small_max"])
+    items, packs = og.plan(sizes, chunk)
     covered = [np.zeros(n, np.int32) if n <= 1 << 24 else None for n in sizes]
     counts = {}
     seen_packed = []
+    seen_chunk = False
     for it in items:
         b, c, t = int(it["begin"]), int(it["count"]), int(it["tensor"])
         assert c > 0
         if t >= 0:
+            seen_chunk = True
             n = sizes[t]
             assert n > lim["small_max"]
-            assert c <= lim["chunk_elems"] and b % 8 == 0 and b + c <= n
+            assert c <= chunk_elems and b % 8 == 0 and b + c <= n
             counts.setdefault(t, []).append((b, c))
             if covered[t] is not None:
                 covered[t][b:b + c] += 1
         else:
+            assert not seen_chunk, "pack items must precede chunk items"
             ids = packs[b:b + c]
             assert c <= lim["pack_max"]
-            assert sum(sizes[i] for i in ids) <= lim["pack_budget"]
+            assert sum(sizes[i] for i in ids) <= pack_budget
             for i in ids:
                 assert 0 < sizes[i] <= lim["small_max"]
                 seen_packed.append(int(i))
@@ -68,8 +73,9 @@ def check_plan(sizes):
             assert b == at
             at += c
         assert at == sizes[t]
-    # chunk items of one tensor are contiguous in the table
+    # chunk items of one tensor are contiguous in the table, tensors in order
     tens = [int(t) for t in items["tensor"] if t >= 0]
+    assert tens == sorted(tens)
     first = {}
     for k, t in enumerate(tens):
         first.setdefault(t, k)
@@ -84,12 +90,15 @@ def check_plan(sizes):
     return items, packs
 
 
+@pytest.mark.parametrize("chunk", [0, 2048, 4096, 12288])
 @pytest.mark.parametrize("sizes", [
     [], [0], [1], [7, 8, 9], [4095, 4096, 4097], [32768, 32769, 65535, 65536, 65537],
     [0, 1, 0, 5000, 0], [3] * 1000, [4096] * 20, [2**31 + 5], [12288 * 36864, 12288, 12288],
 ])
-def test_plan_covers_every_element_once(sizes):
-    check_plan(sizes)
+def test_plan_covers_every_element_once(sizes, chunk):
+    if chunk and sum(sizes) > 1 << 31:
+        pytest.skip("too many items to enumerate quickly")
+    check_plan(sizes, chunk)
 
 
 def test_plan_ragged_config():
@@ -109,6 +118,12 @@ def test_plan_chunks_are_balanced():
     items, _ = og.plan([n])
     counts = sorted(int(c) for c in items["count"])
     assert len(counts) == 4 and counts[-1] - counts[0] <= 8 * len(counts)
+
+
+def test_plan_rejects_bad_chunk_sizes():
+    for chunk in (1024, 2047, 4000, -256):
+        with pytest.raises(og.LambError):
+            og.plan([10000], chunk)
 
 
 def test_plan_rejects_negative_sizes():

@@ -103,6 +103,46 @@ def test_rotating_grad_buffers_match_the_oracle():
         compare_state(st, hs, 1e-4, "after 8 steps", opt, otr)
 
 
+def test_dynamic_loss_scaler_matches_the_oracle():
+    """Device-resident dynamic loss scaling: starting at 2^24, fp16 grads of
+    N(0, 1e-3) overflow, the step skips and the scale backs off; after 3 clean
+    steps it grows again.  Skip flags, the scale sequence (bit-exact) and the
+    state follow the oracle's step and its own scaler rule."""
+    from parity import HostState, compare_state, oracle_step
+    wl = custom([1 << 20, 300000, 4096, 77, 700000], grad_dtype=torch.float16, t0=1, warm=False,
+                S=1.0)
+    st = W.make_state(wl, "cuda")
+    hs = HostState(st, None)
+    flat, views = W.grad_buffer(wl, "cuda")
+    cfg = dict(growth=2.0, backoff=0.5, growth_interval=3, min_scale=1.0, max_scale=2.0 ** 24)
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, grad_dtype=torch.float16) as opt:
+        opt.set_grads(views)
+        opt.set_loss_scaler(init_scale=2.0 ** 24, growth_factor=cfg["growth"],
+                            backoff_factor=cfg["backoff"], growth_interval=3, min_scale=1.0,
+                            max_scale=2.0 ** 24)
+        scale, good, t, skips = 2.0 ** 24, 0, wl.t0, []
+        for k in range(1, 17):
+            assert opt.next_loss_scale == scale
+            W.fill_grads(wl, k, flat, loss_scale=scale)
+            g_host = [W.as_bits(x) for x in views]
+            sk, gn = opt.step(wl.lr, t, 0.0, 12345.0)  # the argument is ignored
+            wl.loss_scale = scale
+            osk, ogn, otr = oracle_step(wl, hs, g_host, t)
+            assert int(sk) == osk and opt.loss_scale == scale
+            skips.append(osk)
+            if not osk:
+                assert_close(np.array([gn]), np.array([ogn]), 1e-4, f"step {k} grad_norm")
+                t += 1
+            scale, good = oracle.loss_scale_update(scale, good, osk, **cfg)
+            assert opt.next_loss_scale == scale, (k, opt.next_loss_scale, scale)
+            if k in (4, 16):
+                compare_state(st, hs, 1e-4, f"step {k}", opt, None)
+        assert skips[0] == 1 and sum(skips) >= 3 and 0 in skips
+        opt.clear_loss_scaler()
+        W.fill_grads(wl, 17, flat, loss_scale=1024.0)
+        assert opt.step(wl.lr, t, 0.0, 1024.0)[0] is False and opt.loss_scale == 1024.0
+
+
 def test_deterministic_across_runs():
     wl = custom([300001, 17, 5000, 123])
     outs = []

@@ -372,3 +372,41 @@ def test_rejects_bad_arguments():
                dict(loss_scale=math.inf)):
         with pytest.raises(ValueError):
             run(copy_state(st), [1], **kw)
+
+
+# ------------------------------------------------- dynamic loss scaling
+@pytest.mark.parametrize("growth,backoff,interval", [(2.0, 0.5, 3), (2.0, 0.5, 1), (1.5, 0.25, 5),
+                                                     (4.0, 0.5, 2000)])
+def test_loss_scale_update_matches_torch(growth, backoff, interval):
+    """The oracle's scaler agrees with torch's own update routine (no clamps)."""
+    rng = np.random.default_rng(int(growth * 10 + interval))
+    flags = (rng.random(400) < 0.15).astype(int)
+    flags[50:80] = 0
+    s_t = torch.tensor([65536.0])
+    g_t = torch.tensor([0], dtype=torch.int32)
+    f_t = torch.tensor([0.0])
+    s, g = 65536.0, 0
+    for f in flags:
+        f_t.fill_(float(f))
+        torch._amp_update_scale_(s_t, g_t, f_t, growth, backoff, interval)
+        s, g = oracle.loss_scale_update(s, g, f, growth=growth, backoff=backoff,
+                                        growth_interval=interval)
+        assert s == s_t.item() and g == g_t.item()
+
+
+def test_loss_scale_update_hand_sequence_with_clamps():
+    """Interval 2, x2 / x0.5, clamped to [1, 8]; written out by hand."""
+    flags = [0, 0, 0, 0, 0, 0, 1, 1, 1, 1, 0, 0]
+    want = [(2.0, 1), (4.0, 0), (4.0, 1), (8.0, 0), (8.0, 1), (8.0, 0),
+            (4.0, 0), (2.0, 0), (1.0, 0), (1.0, 0), (1.0, 1), (2.0, 0)]
+    s, g = 2.0, 0
+    for f, w in zip(flags, want):
+        s, g = oracle.loss_scale_update(s, g, f, growth=2.0, backoff=0.5, growth_interval=2,
+                                        min_scale=1.0, max_scale=8.0)
+        assert (s, g) == w
+
+
+def test_loss_scale_growth_never_overflows():
+    s, g = 3.0e38, 0
+    s, g = oracle.loss_scale_update(s, g, 0, growth=2.0, backoff=0.5, growth_interval=1)
+    assert s == np.float32(3.0e38) and g == 0

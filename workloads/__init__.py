@@ -257,9 +257,13 @@ def injection_site(wl: Workload, step: int) -> Optional[Tuple[int, int, str]]:
     return ti, int(rng.integers(wl.sizes[ti])), wl.inject[step]
 
 
-def fill_grads(wl: Workload, step: int, flat: torch.Tensor) -> None:
-    """Grads of step ``step`` (1-based index in a run) into ``flat``."""
-    mult = wl.loss_scale if wl.grad_dtype == torch.float16 else 1.0
+def fill_grads(wl: Workload, step: int, flat: torch.Tensor, loss_scale: float = None) -> None:
+    """Grads of step ``step`` (1-based index in a run) into ``flat``; fp16
+    grads carry the loss scale (``loss_scale`` if given, else the config's)."""
+    if wl.grad_dtype == torch.float16:
+        mult = wl.loss_scale if loss_scale is None else float(loss_scale)
+    else:
+        mult = 1.0
     _fill_grads(flat, wl.grad_kind, wl.grad_sigma, mult, wl.seed, 10, step)
     site = injection_site(wl, step)
     if site is not None:
