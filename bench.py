@@ -74,6 +74,9 @@ def parse_args(argv=None):
                    help="cut every tensor to at most this many elements (small cases for "
                         "profiling); 0 = the full workload")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--snapshot", action="store_true",
+                   help="also time the state snapshot into pinned host memory (the first "
+                        "stage of a checkpoint) and a step issued while it runs")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU oracle budget for the cpu_baseline sample")
@@ -356,6 +359,29 @@ def run_ours(args, world, rank, local):
                "pipeline": "double-buffered grads; H2D of step k+1 overlaps step k"}
         del pinned, gflat2, gv2, bufs, views
 
+    # ---- state snapshot into pinned host memory (checkpoint stage 1)
+    snap = None
+    if args.snapshot:
+        host = [[torch.empty(n, dtype=torch.float32, pin_memory=True) for n in wl.sizes]
+                for _ in range(3)]
+        opt.set_grads(gv)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        opt.snapshot_async(*host)
+        opt.snapshot_wait()
+        alone = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        opt.snapshot_async(*host)
+        step()                      # its state-writing kernels wait on the GPU
+        opt.snapshot_wait()
+        both = time.perf_counter() - t0
+        nbytes = 12 * N
+        snap = {"bytes": nbytes, "ms": round(alone * 1e3, 2),
+                "GB/s": round(nbytes / alone / 1e9, 1),
+                "ms_snapshot_then_step": round(both * 1e3, 2),
+                "ms_step_alone": round(step_ms, 3)}
+        del host
+
     opt.close()
     del st, gflat, gv
     cpu = None
@@ -394,6 +420,8 @@ def run_ours(args, world, rank, local):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if snap is not None:
+            out["snapshot"] = snap
         print(json.dumps(out), flush=True)
 
 

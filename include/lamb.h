@@ -184,6 +184,29 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
  */
 LAMB_API int lamb_set_loss_scaler(lamb_handle* h, const lamb_loss_scaler* cfg);
 
+/*
+ * Snapshot of the optimizer state into host memory: the first stage of
+ * MegaScale's two-stage checkpoint (guided-reading digest, section 6: copy
+ * each GPU's state to pinned host memory in seconds, then write it to
+ * storage in the background).
+ *
+ *   host_w, host_m, host_v  host arrays of n_tensors host pointers that
+ *                receive each tensor's fp32 w, m and v (size n_i floats;
+ *                page-locked memory makes the copies asynchronous)
+ *   stream       the cudaStream_t the copies are enqueued on, normally one
+ *                other than the handle's so that they overlap other work
+ *
+ * The copies start once everything already enqueued on the handle's stream
+ * has finished, so they capture the state between two steps.  The call
+ * returns at once.  The next lamb_step makes its state-writing kernels wait
+ * for the copies on the GPU (its grad-norm kernel still overlaps them), so a
+ * step never changes the state under a running snapshot; no host wait is
+ * needed.  lamb_snapshot_wait blocks until the copies are in host memory.
+ */
+LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* const* host_m,
+                                 float* const* host_v, void* stream);
+LAMB_API int lamb_snapshot_wait(lamb_handle* h);
+
 /* Free everything the handle owns (after waiting for its stream).  NULL is a
  * no-op.  Caller-owned buffers are untouched. */
 LAMB_API int lamb_destroy(lamb_handle* h);

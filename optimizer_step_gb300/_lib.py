@@ -23,7 +23,8 @@ LAMB_GRAD_FP16 = 1
 # Every symbol include/lamb.h declares.
 EXPORTS = ("lamb_create", "lamb_step", "lamb_destroy", "lamb_last_error", "lamb_get_trust",
            "lamb_set_timing", "lamb_kernel_times", "lamb_plan", "lamb_plan_limits",
-           "lamb_set_loss_scaler", "lamb_grad_norm_noalloc")
+           "lamb_set_loss_scaler", "lamb_snapshot_async", "lamb_snapshot_wait",
+           "lamb_grad_norm_noalloc")
 
 
 class LambHParams(ctypes.Structure):
@@ -87,6 +88,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.lamb_get_trust.argtypes = [P, P, i32]
         lib.lamb_set_loss_scaler.restype = ctypes.c_int
         lib.lamb_set_loss_scaler.argtypes = [P, ctypes.POINTER(LambLossScaler)]
+        lib.lamb_snapshot_async.restype = ctypes.c_int
+        lib.lamb_snapshot_async.argtypes = [P, P, P, P, P]
+        lib.lamb_snapshot_wait.restype = ctypes.c_int
+        lib.lamb_snapshot_wait.argtypes = [P]
         lib.lamb_set_timing.restype = ctypes.c_int
         lib.lamb_set_timing.argtypes = [P, i32]
         lib.lamb_kernel_times.restype = ctypes.c_int

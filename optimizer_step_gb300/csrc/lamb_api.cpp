@@ -69,6 +69,10 @@ struct lamb_handle {
   DevTables T{};
   int grid[3] = {0, 0, 0};
   ScaleArgs scaler{};         // dynamic == 1 while a dynamic loss scaler is on
+  std::vector<TensorDesc> td_host;       // the tensors' device pointers
+  cudaEvent_t snap_start = nullptr;      // handle stream: state is between steps
+  cudaEvent_t snap_done = nullptr;       // snapshot stream: copies finished
+  bool snap_pending = false;             // the next step must wait for snap_done
   bool timing = false;        // CUDA event monitor on
   bool timed_step = false;    // a step has been timed since it was turned on
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -169,6 +173,7 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
     td[i].pad = 0;
   }
   std::vector<float> ones(nt, 1.0f);
+  h->td_host = td;
 
   // One device allocation, carved into 256-byte aligned regions.
   size_t off = 0;
@@ -305,6 +310,13 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   sa.fixed = loss_scale;
   int rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, clip, sa, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
+  if (h->snap_pending) {
+    // A snapshot of the state taken before this step may still be copying:
+    // the kernels that write the state wait for it (on the GPU only).
+    if ((ce = cudaStreamWaitEvent(h->stream, h->snap_done, 0)) != cudaSuccess)
+      return cuda_fail(ce, "waiting for the snapshot copies");
+    h->snap_pending = false;
+  }
   if ((ce = mark(h, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
   rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
@@ -400,6 +412,53 @@ LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms) {
   return LAMB_OK;
 }
 
+LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* const* host_m,
+                                 float* const* host_v, void* stream) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (h->n_tensors > 0 && (!host_w || !host_m || !host_v))
+    return fail(LAMB_ERR_INVALID, "host pointer arrays must be non-NULL");
+  for (int32_t i = 0; i < h->n_tensors; ++i) {
+    if (h->td_host[size_t(i)].n > 0 && (!host_w[i] || !host_m[i] || !host_v[i]))
+      return fail(LAMB_ERR_INVALID, "tensor " + std::to_string(i) + " has a NULL host pointer");
+  }
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  cudaError_t ce = cudaSuccess;
+  if (!h->snap_start) ce = cudaEventCreateWithFlags(&h->snap_start, cudaEventDisableTiming);
+  if (ce == cudaSuccess && !h->snap_done)
+    ce = cudaEventCreateWithFlags(&h->snap_done, cudaEventDisableTiming);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreate");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // Copies start once everything enqueued on the handle's stream is done.
+  if ((ce = cudaEventRecord(h->snap_start, h->stream)) != cudaSuccess ||
+      (ce = cudaStreamWaitEvent(cs, h->snap_start, 0)) != cudaSuccess)
+    return cuda_fail(ce, "ordering the snapshot after the last step");
+  for (int32_t i = 0; i < h->n_tensors; ++i) {
+    const TensorDesc& d = h->td_host[size_t(i)];
+    if (d.n == 0) continue;
+    const size_t bytes = size_t(d.n) * sizeof(float);
+    if ((ce = cudaMemcpyAsync(host_w[i], d.w, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess ||
+        (ce = cudaMemcpyAsync(host_m[i], d.m, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess ||
+        (ce = cudaMemcpyAsync(host_v[i], d.v, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
+      return cuda_fail(ce, "enqueueing snapshot copies");
+  }
+  if ((ce = cudaEventRecord(h->snap_done, cs)) != cudaSuccess)
+    return cuda_fail(ce, "event record");
+  h->snap_pending = true;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_snapshot_wait(lamb_handle* h) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (!h->snap_done) return LAMB_OK;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  const cudaError_t ce = cudaEventSynchronize(h->snap_done);
+  return ce == cudaSuccess ? LAMB_OK : cuda_fail(ce, "waiting for the snapshot");
+}
+
 LAMB_API int lamb_get_trust(lamb_handle* h, float* host_out, int32_t n_tensors) {
   g_last_error.clear();
   if (!h || !host_out) return fail(LAMB_ERR_INVALID, "NULL argument");
@@ -423,6 +482,11 @@ LAMB_API int lamb_destroy(lamb_handle* h) {
     cudaError_t ce = cudaStreamSynchronize(h->stream);
     if (ce != cudaSuccess) rc = cuda_fail(ce, "waiting for the stream");
     destroy_events(h);
+    if (h->snap_done) {
+      cudaEventSynchronize(h->snap_done);
+      cudaEventDestroy(h->snap_done);
+    }
+    if (h->snap_start) cudaEventDestroy(h->snap_start);
     if (h->pinned) cudaFreeHost(h->pinned);
     if (h->dev_block) cudaFree(h->dev_block);
   }

@@ -138,6 +138,30 @@ class Lamb:
         check(self._lib.lamb_get_trust(self._h, out.ctypes.data, self._n))
         return out[: self._n]
 
+    def snapshot_async(self, host_w, host_m, host_v, stream=None) -> None:
+        """Copy every tensor's w, m, v into host tensors (page-locked for an
+        asynchronous copy) on ``stream`` (default: a stream of this object's
+        own).  The next ``step`` waits on the GPU for the copies before it
+        writes the state; ``snapshot_wait`` blocks until they are done."""
+        for name, lst in (("host_w", host_w), ("host_m", host_m), ("host_v", host_v)):
+            if len(lst) != self._n:
+                raise ValueError(f"{name}: expected {self._n} tensors")
+            for t, n in zip(lst, self.sizes):
+                if (not isinstance(t, torch.Tensor) or t.device.type != "cpu"
+                        or t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != n):
+                    raise ValueError(f"{name}: need contiguous fp32 CPU tensors of the "
+                                     f"state's sizes")
+        if stream is None:
+            if getattr(self, "_snap_stream", None) is None:
+                self._snap_stream = torch.cuda.Stream(device=self.device)
+            stream = self._snap_stream
+        self._snap_keep = (list(host_w), list(host_m), list(host_v))
+        check(self._lib.lamb_snapshot_async(self._h, _ptrs(host_w), _ptrs(host_m),
+                                            _ptrs(host_v), ctypes.c_void_p(stream.cuda_stream)))
+
+    def snapshot_wait(self) -> None:
+        check(self._lib.lamb_snapshot_wait(self._h))
+
     def set_timing(self, enable: bool = True) -> None:
         """Turn the library's CUDA event monitor on or off."""
         check(self._lib.lamb_set_timing(self._h, 1 if enable else 0))

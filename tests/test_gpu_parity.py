@@ -143,6 +143,45 @@ def test_dynamic_loss_scaler_matches_the_oracle():
         assert opt.step(wl.lr, t, 0.0, 1024.0)[0] is False and opt.loss_scale == 1024.0
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_snapshot_captures_the_state_between_steps(pinned):
+    """A snapshot taken after step 2 holds exactly the state after step 2, even
+    though step 3 is enqueued at once; and step 3 is bit-identical to a run
+    without a snapshot."""
+    wl = custom([70001, 17, 5000, 1 << 20, 0, 300], t0=4, clip=0.02)
+    st = W.make_state(wl, "cuda")
+    ref = st.clone()
+    flat, views = W.grad_buffer(wl, "cuda")
+
+    def run(state, snapshot):
+        with Lamb(state.w, state.m, state.v, state.w16, wl.wd_flags) as opt:
+            opt.set_grads(views)
+            for k in (1, 2):
+                W.fill_grads(wl, k, flat)
+                opt.step(wl.lr, wl.t0 + k - 1, wl.clip)
+            if not snapshot:
+                W.fill_grads(wl, 3, flat)
+                opt.step(wl.lr, wl.t0 + 2, wl.clip)
+                return None
+            expect = [x.clone() for x in (state.w_flat, state.m_flat, state.v_flat)]
+            host = [[torch.empty(n, dtype=torch.float32, pin_memory=pinned) for n in wl.sizes]
+                    for _ in range(3)]
+            opt.snapshot_async(*host)
+            W.fill_grads(wl, 3, flat)
+            opt.step(wl.lr, wl.t0 + 2, wl.clip)
+            opt.snapshot_wait()
+            return expect, host
+
+    run(ref, False)
+    expect, host = run(st, True)
+    for flat_exp, views_host in zip(expect, host):
+        for o, n, h in zip(W.offsets(wl.sizes)[0], wl.sizes, views_host):
+            assert torch.equal(flat_exp[o:o + n].cpu().view(torch.int32), h.view(torch.int32))
+    for a, b in ((st.w_flat, ref.w_flat), (st.m_flat, ref.m_flat), (st.v_flat, ref.v_flat),
+                 (st.w16_flat, ref.w16_flat)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 def test_deterministic_across_runs():
     wl = custom([300001, 17, 5000, 123])
     outs = []
