@@ -219,7 +219,10 @@ struct ItemQueue {
 // kLoadsA 16-byte loads in flight and sums at most 128 squares in fp32 before
 // folding them into fp64 (a chunk gives each thread at most 16 vectors; a
 // packed tensor of at most 4096 elements gives each lane at most 16).
-constexpr int kLoadsA = 4;
+#ifndef LAMB_LOADS_A
+#define LAMB_LOADS_A 4
+#endif
+constexpr int kLoadsA = LAMB_LOADS_A;
 
 template <int DT>
 __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int64_t n, int tid,

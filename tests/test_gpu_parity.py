@@ -148,7 +148,10 @@ def test_snapshot_captures_the_state_between_steps(pinned):
     """A snapshot taken after step 2 holds exactly the state after step 2, even
     though step 3 is enqueued at once; and step 3 is bit-identical to a run
     without a snapshot."""
-    wl = custom([70001, 17, 5000, 1 << 20, 0, 300], t0=4, clip=0.02)
+    # 128M elements: 1.5 GB of state, many milliseconds of copies, far longer
+    # than the next step's grad-norm kernel, so a step that did not wait would
+    # be caught rewriting m and v under the copy.
+    wl = custom([70001, 17, 5000, 1 << 27, 0, 300], t0=4, clip=0.02)
     st = W.make_state(wl, "cuda")
     ref = st.clone()
     flat, views = W.grad_buffer(wl, "cuda")
@@ -180,6 +183,52 @@ def test_snapshot_captures_the_state_between_steps(pinned):
     for a, b in ((st.w_flat, ref.w_flat), (st.m_flat, ref.m_flat), (st.v_flat, ref.v_flat),
                  (st.w16_flat, ref.w16_flat)):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_bf16_copies_land_in_one_allgather_bucket():
+    """The bf16 copies can be written straight into a ZeRO-2 all-gather bucket:
+    one contiguous bf16 buffer with the tensors back to back at 16-byte
+    aligned offsets.  After two steps the bucket holds exactly bf16(w) of every
+    tensor, and the padding between tensors is untouched."""
+    wl = custom([1000, 8, 4096, 70001, 3, 130], t0=2, clip=0.05)
+    st = W.make_state(wl, "cuda")
+    offs, at = [], 0
+    for n in wl.sizes:
+        offs.append(at)
+        at += (n + 7) // 8 * 8
+    sentinel = 0x7FC1  # a NaN pattern no weight rounds to
+    bucket = torch.full((at,), sentinel, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    views16 = [bucket[o:o + n] for o, n in zip(offs, wl.sizes)]
+    flat, gv = W.grad_buffer(wl, "cuda")
+    with Lamb(st.w, st.m, st.v, views16, wl.wd_flags) as opt:
+        for k in (1, 2):
+            W.fill_grads(wl, k, flat)
+            opt.step(wl.lr, wl.t0 + k - 1, wl.clip, grads=gv)
+    bits = bucket.view(torch.int16).cpu().numpy().view(np.uint16)
+    covered = np.zeros(at, bool)
+    for o, n, w in zip(offs, wl.sizes, st.w):
+        assert np.array_equal(bits[o:o + n], oracle.bf16_rne(W.as_f32(w)))
+        covered[o:o + n] = True
+    assert np.all(bits[~covered] == sentinel)
+
+
+@pytest.mark.parametrize("case", [
+    dict(beta1=0.0, beta2=0.0),            # m = g', v = g'^2 exactly
+    dict(lr=0.0),                          # w unchanged, m and v still updated
+    dict(t0=10_000_000),                   # b^t underflows: no bias correction
+    dict(weight_decay=0.0),                # the decay term vanishes everywhere
+    dict(beta1=0.5, beta2=0.75, eps=0.5),  # large eps dominates sqrt(v)
+    dict(sigma=3.0e4),                     # bf16 grads near 1e5 (large squares)
+    dict(sigma=1e-15),                     # tiny grads: squares near 1e-30
+])
+def test_hyperparameter_corner_cases(case):
+    case = dict(case)
+    hp = {k: case.pop(k) for k in ("beta1", "beta2", "eps", "weight_decay", "lr") if k in case}
+    wl = custom([70001, 4096, 17, 300000], t0=case.pop("t0", 3), sigma=case.pop("sigma", 1e-3),
+                clip=1.0)
+    for k, v in hp.items():
+        setattr(wl, k, v)
+    run_parity(wl, 3, check_steps=(1, 3))
 
 
 def test_deterministic_across_runs():
@@ -290,6 +339,13 @@ def test_config_175b_shard_full_step():
 def test_config_175b_shard_ten_steps_subset():
     wl = W.shard175b()
     run_parity(wl, 10, check_steps=(1, 10), subset=[1, 4, 5])
+
+
+def test_tensor_larger_than_2_to_the_31_elements():
+    """64-bit element offsets: one tensor of 2^31 + 5 elements (plus a small one),
+    checked in full against the oracle after one step."""
+    wl = custom([(1 << 31) + 5, 1000], t0=7, clip=1.0, sigma=1e-4)
+    _large_one_step(wl, [0, 1])
 
 
 def test_config_7b_one_step_and_ten_steps_subset():
