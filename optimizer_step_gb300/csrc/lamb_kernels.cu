@@ -80,18 +80,57 @@ constexpr int kWarps = kThreads / 32;
 
 // ------------------------------------------------------------ memory access
 // Everything is streamed once per kernel and the step's footprint is far
-// larger than L2, so loads and stores are marked evict-first (.cs).
+// larger than L2.  LAMB_LD_POLICY / LAMB_ST_POLICY pick the cache policy of
+// the 128-bit accesses (tuning sweeps): loads 0 evict-first (.cs), 1 default,
+// 2 cache-global (.cg), 3 last-use (.lu), 4 default with a 256-byte L2
+// prefetch; stores 0 evict-first (.cs), 1 default (write-back), 2 .cg.
+#ifndef LAMB_LD_POLICY
+#define LAMB_LD_POLICY 0
+#endif
+#ifndef LAMB_ST_POLICY
+#define LAMB_ST_POLICY 0
+#endif
+template <class T>
+__device__ __forceinline__ T ld_policy(const T* p) {
+#if LAMB_LD_POLICY == 0
+  return __ldcs(p);
+#elif LAMB_LD_POLICY == 1
+  return *p;
+#elif LAMB_LD_POLICY == 2
+  return __ldcg(p);
+#elif LAMB_LD_POLICY == 3
+  return __ldlu(p);
+#else
+  T r;
+  static_assert(sizeof(T) == 16, "128-bit accesses only");
+  uint32_t* q = reinterpret_cast<uint32_t*>(&r);
+  asm volatile("ld.global.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+               : "l"(p));
+  return r;
+#endif
+}
+template <class T>
+__device__ __forceinline__ void st_policy(T* p, T x) {
+#if LAMB_ST_POLICY == 0
+  __stcs(p, x);
+#elif LAMB_ST_POLICY == 1
+  *p = x;
+#else
+  __stcg(p, x);
+#endif
+}
 __device__ __forceinline__ uint4 ld_u4(const void* p) {
-  return __ldcs(reinterpret_cast<const uint4*>(p));
+  return ld_policy(reinterpret_cast<const uint4*>(p));
 }
 __device__ __forceinline__ float4 ld_f4(const float* p) {
-  return __ldcs(reinterpret_cast<const float4*>(p));
+  return ld_policy(reinterpret_cast<const float4*>(p));
 }
 __device__ __forceinline__ void st_f4(float* p, float4 x) {
-  __stcs(reinterpret_cast<float4*>(p), x);
+  st_policy(reinterpret_cast<float4*>(p), x);
 }
 __device__ __forceinline__ void st_u4(void* p, uint4 x) {
-  __stcs(reinterpret_cast<uint4*>(p), x);
+  st_policy(reinterpret_cast<uint4*>(p), x);
 }
 
 // ----------------------------------------------------------- grad decoding
