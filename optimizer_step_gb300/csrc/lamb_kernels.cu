@@ -25,9 +25,11 @@
 // instead of m and v), and avoids a 4 B/param scratch buffer.
 //
 // Work is split by the host-built table of work items (chunks of large
-// tensors; packs of small tensors, a warp per tensor).  Grids are persistent:
-// each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
-// Every reduction has a fixed order, so results are deterministic run to run.
+// tensors; packs of small tensors, a warp per tensor).  Grids are persistent
+// (a few CTAs per SM): the grad-norm kernel's CTAs walk items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the moments and apply kernels take items
+// greedily from an atomic counter, which balanced better on GB300.  Every
+// reduction has a fixed order, so results are deterministic run to run.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

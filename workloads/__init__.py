@@ -120,7 +120,7 @@ def fp16_24() -> Workload:
                     grad_sigma=1e-3, seed=1005, inject={7: "inf", 15: "nan"})
 
 
-CONFIGS = {"tiny": tiny, "shard175b": shard175b, "ragged": ragged, "7b": llama7b,
+WORKLOADS = {"tiny": tiny, "shard175b": shard175b, "ragged": ragged, "7b": llama7b,
            "fp16": fp16_24}
 
 
