@@ -268,6 +268,35 @@ def test_empty_handle_and_errors():
     assert e.value.code == -2
 
 
+def test_scaler_snapshot_and_monitor_argument_errors():
+    import ctypes
+    from optimizer_step_gb300 import _lib
+    wl = custom([64, 5000])
+    st = W.make_state(wl, "cuda")
+    _, gv = W.make_grads(wl, 1, "cuda")
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags) as opt:
+        with pytest.raises(LambError):
+            opt.kernel_times()  # monitor off
+        opt.set_timing(True)
+        with pytest.raises(LambError):
+            opt.kernel_times()  # no step timed yet
+        opt.step(1e-3, 1, grads=gv)
+        assert all(x > 0 for x in opt.kernel_times())
+        for bad in (dict(init_scale=0.0), dict(init_scale=float("inf")), dict(growth_factor=0.5),
+                    dict(backoff_factor=0.0), dict(backoff_factor=1.5), dict(growth_interval=0),
+                    dict(min_scale=2.0 ** 20, init_scale=2.0 ** 10),
+                    dict(max_scale=2.0, init_scale=4.0)):
+            with pytest.raises(LambError) as e:
+                opt.set_loss_scaler(**bad)
+            assert e.value.code == _lib.LAMB_ERR_INVALID
+        with pytest.raises(ValueError):
+            opt.snapshot_async([torch.empty(3)], [torch.empty(3)], [torch.empty(3)])
+        lib = _lib.load()
+        null = (ctypes.c_void_p * 2)(None, None)
+        assert lib.lamb_snapshot_async(opt._h, null, null, null, None) == _lib.LAMB_ERR_INVALID
+        opt.snapshot_wait()  # nothing pending: returns at once
+
+
 # ------------------------------------------------------- the named configs
 def test_config_tiny_one_and_ten_steps():
     log = run_parity(W.tiny(), 10, check_steps=(1, 10))
