@@ -201,7 +201,9 @@ LAMB_API int lamb_set_loss_scaler(lamb_handle* h, const lamb_loss_scaler* cfg);
  * returns at once.  The next lamb_step makes its state-writing kernels wait
  * for the copies on the GPU (its grad-norm kernel still overlaps them), so a
  * step never changes the state under a running snapshot; no host wait is
- * needed.  lamb_snapshot_wait blocks until the copies are in host memory.
+ * needed.  Several snapshots may be outstanding at once (on any streams):
+ * the next step waits for all of them.  lamb_snapshot_wait blocks until every
+ * outstanding copy is in host memory.
  */
 LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* const* host_m,
                                  float* const* host_v, void* stream);

@@ -434,6 +434,10 @@ LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* co
   if ((ce = cudaEventRecord(h->snap_start, h->stream)) != cudaSuccess ||
       (ce = cudaStreamWaitEvent(cs, h->snap_start, 0)) != cudaSuccess)
     return cuda_fail(ce, "ordering the snapshot after the last step");
+  // A snapshot still pending (perhaps on another stream) is chained in, so
+  // that snap_done below covers every outstanding copy.
+  if (h->snap_pending && (ce = cudaStreamWaitEvent(cs, h->snap_done, 0)) != cudaSuccess)
+    return cuda_fail(ce, "ordering after the previous snapshot");
   for (int32_t i = 0; i < h->n_tensors; ++i) {
     const TensorDesc& d = h->td_host[size_t(i)];
     if (d.n == 0) continue;

@@ -155,12 +155,17 @@ class Lamb:
             if getattr(self, "_snap_stream", None) is None:
                 self._snap_stream = torch.cuda.Stream(device=self.device)
             stream = self._snap_stream
-        self._snap_keep = (list(host_w), list(host_m), list(host_v))
+        # The host tensors must outlive their copies: keep every outstanding set.
+        if getattr(self, "_snap_keep", None) is None:
+            self._snap_keep = []
+        self._snap_keep.append((list(host_w), list(host_m), list(host_v)))
         check(self._lib.lamb_snapshot_async(self._h, _ptrs(host_w), _ptrs(host_m),
                                             _ptrs(host_v), ctypes.c_void_p(stream.cuda_stream)))
 
     def snapshot_wait(self) -> None:
+        """Block until every outstanding snapshot is in host memory."""
         check(self._lib.lamb_snapshot_wait(self._h))
+        self._snap_keep = []
 
     def set_timing(self, enable: bool = True) -> None:
         """Turn the library's CUDA event monitor on or off."""

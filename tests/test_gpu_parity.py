@@ -231,6 +231,27 @@ def test_hyperparameter_corner_cases(case):
     run_parity(wl, 3, check_steps=(1, 3))
 
 
+def test_two_snapshots_on_two_streams_both_precede_the_next_step():
+    wl = custom([1 << 26, 5000, 17], t0=2)
+    st = W.make_state(wl, "cuda")
+    _, gv = W.make_grads(wl, 1, "cuda")
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags) as opt:
+        opt.step(wl.lr, wl.t0, grads=gv)
+        expect = [x.clone() for x in (st.w_flat, st.m_flat, st.v_flat)]
+        sets = [[[torch.empty(n, dtype=torch.float32, pin_memory=True) for n in wl.sizes]
+                 for _ in range(3)] for _ in range(2)]
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        opt.snapshot_async(*sets[0], stream=s1)
+        opt.snapshot_async(*sets[1], stream=s2)
+        opt.step(wl.lr, wl.t0 + 1, grads=gv)  # must wait for both
+        opt.snapshot_wait()
+    offs = W.offsets(wl.sizes)[0]
+    for host in sets:
+        for flat_exp, views_host in zip(expect, host):
+            for o, n, h in zip(offs, wl.sizes, views_host):
+                assert torch.equal(flat_exp[o:o + n].cpu().view(torch.int32), h.view(torch.int32))
+
+
 def test_deterministic_across_runs():
     wl = custom([300001, 17, 5000, 123])
     outs = []
