@@ -248,9 +248,10 @@ LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms);
  * 1 .. small_max elements are packed whole, in order, into packs of at most
  * max(chunk_elems, small_max) elements and pack_max tensors; empty tensors
  * get no work.  Pack items come first, then each large tensor's chunks,
- * contiguous and in tensor order.  lamb_create picks chunk_elems itself: the
- * largest chunk (at most 32768) that still gives every resident CTA of the
- * GPU about 8 items, and never below 2048.
+ * contiguous and in tensor order.  lamb_create picks chunk_elems itself:
+ * the fewest whole waves of one item per resident CTA of the GPU that keep
+ * chunks at most 32768 elements, and the chunk size that fills them (never
+ * below 2048).
  *
  *   chunk_elems             0 (= 32768) or a multiple of 256 in [2048, 2^30]
  *   items, items_cap        output array for the work items (may be NULL)

@@ -17,13 +17,12 @@ namespace lambgb {
 // alignment of the fp32 and 16-bit arrays); tensors up to kSmallMax elements
 // are packed whole, one warp per tensor, at most max(chunk_elems, kSmallMax)
 // elements and kPackMax tensors a pack.  lamb_create picks chunk_elems from
-// the shard size and the GPU (choose_chunk), so that small shards still give
-// every resident CTA several items; kChunkElems is the largest value.
+// the shard size and the GPU (choose_chunk): whole waves of one item per
+// resident CTA; kChunkElems is the largest value.
 constexpr int64_t kChunkElems = 32768;
 constexpr int64_t kMinChunkElems = 2048;
 constexpr int64_t kSmallMax = 4096;
 constexpr int64_t kPackMax = 64;
-constexpr int64_t kItemsPerSlot = 8;  // target work items per resident CTA
 
 // Chunk size for n_params elements on a GPU with cta_slots resident CTAs.
 int64_t choose_chunk(int64_t n_params, int64_t cta_slots);

@@ -16,10 +16,17 @@
 
 namespace lambgb {
 
+// Whole waves of work: the fewest rounds of one item per resident CTA that
+// keep chunks at most kChunkElems, and the chunk size that fills them.  Small
+// shards then give each CTA one or two large items instead of several small
+// ones, which matters because each item costs a chain of dependent latencies
+// (table, data, block reduction, ticket); large shards get full-size chunks.
 int64_t choose_chunk(int64_t n_params, int64_t cta_slots) {
-  const int64_t target = std::max<int64_t>(1, cta_slots) * kItemsPerSlot;
-  int64_t c = (n_params + target - 1) / target;
-  c = (c + kMinChunkElems - 1) / kMinChunkElems * kMinChunkElems;
+  const int64_t slots = std::max<int64_t>(1, cta_slots);
+  const int64_t waves = std::max<int64_t>(1, (n_params + slots * kChunkElems - 1) /
+                                                 (slots * kChunkElems));
+  int64_t c = (n_params + waves * slots - 1) / (waves * slots);
+  c = (c + 255) / 256 * 256;
   return std::min(kChunkElems, std::max(kMinChunkElems, c));
 }
 
