@@ -161,13 +161,16 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
  *   clip        global grad-norm clip threshold; <= 0 disables clipping
  *   loss_scale  S > 0 (finite); grads are divided by S (ignored while a
  *               dynamic loss scaler is on)
- *   out         receives {skipped, grad_norm}
+ *   out         receives {skipped, grad_norm, loss_scale, next_loss_scale}
  *
  * Enqueues three kernels on the handle's stream (grad norm, moments and
  * per-tensor norms, apply), then copies the small outcome record to pinned
  * host memory and waits for it: the call returns when the step has finished
  * on the GPU.  The skip decision is taken on the GPU; the host never reads it in
- * the middle of a step.
+ * the middle of a step.  Each step's grad-pointer set is matched against four
+ * device slots, so alternating among up to four grad buffers costs no upload;
+ * a new set is written by a small kernel, never by a copy (a copy could queue
+ * behind unrelated bulk transfers on the copy engine).
  */
 LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
                        float loss_scale, lamb_result* out);
