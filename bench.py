@@ -471,6 +471,11 @@ def main(argv=None):
         run_reference(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.barrier()
+                dist.destroy_process_group()
 
 
 if __name__ == "__main__":
