@@ -252,6 +252,35 @@ def test_two_snapshots_on_two_streams_both_precede_the_next_step():
                 assert torch.equal(flat_exp[o:o + n].cpu().view(torch.int32), h.view(torch.int32))
 
 
+def test_handle_on_a_side_stream():
+    """A handle bound to a non-default stream: grads produced on that stream
+    are consumed in order, and the results match the oracle."""
+    from parity import HostState, compare_state, oracle_step
+    wl = custom([70001, 300, 4096], t0=6, clip=0.05)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        st = W.make_state(wl, "cuda")
+        hs = HostState(st, None)
+        flat, views = W.grad_buffer(wl, "cuda")
+        opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags)
+        assert opt.stream.cuda_stream == side.cuda_stream
+        W.fill_grads(wl, 1, flat)  # enqueued on the side stream
+        sk, gn = opt.step(wl.lr, wl.t0, wl.clip, grads=views)
+    g_host = [W.as_bits(x) for x in views]
+    osk, ogn, otr = oracle_step(wl, hs, g_host, wl.t0)
+    assert not sk and not osk
+    assert_close(np.array([gn]), np.array([ogn]), 1e-5, "grad_norm")
+    compare_state(st, hs, 1e-5, "side stream", opt, otr)
+    opt.close()
+
+
+def test_twenty_thousand_tiny_tensors():
+    """The pack path and the pointer-write kernel at scale: 20,000 tensors of
+    1 to 64 elements (313 packs, 42 pointer-write launches)."""
+    sizes = [int(x) for x in np.random.default_rng(9).integers(1, 65, 20000)]
+    run_parity(custom(sizes, t0=2, clip=0.01), 3, check_steps=(1, 3))
+
+
 def test_deterministic_across_runs():
     wl = custom([300001, 17, 5000, 123])
     outs = []

@@ -198,21 +198,27 @@ class State:
     def views(self, flat: torch.Tensor) -> List[torch.Tensor]:
         return [flat[o:o + n] for o, n in zip(self.offsets, self.wl.sizes)]
 
+    def _cached(self, name: str, flat: torch.Tensor) -> List[torch.Tensor]:
+        cache = self.__dict__.setdefault("_views", {})
+        if name not in cache:
+            cache[name] = self.views(flat)
+        return cache[name]
+
     @property
     def w(self):
-        return self.views(self.w_flat)
+        return self._cached("w", self.w_flat)
 
     @property
     def m(self):
-        return self.views(self.m_flat)
+        return self._cached("m", self.m_flat)
 
     @property
     def v(self):
-        return self.views(self.v_flat)
+        return self._cached("v", self.v_flat)
 
     @property
     def w16(self):
-        return self.views(self.w16_flat)
+        return self._cached("w16", self.w16_flat)
 
     def clone(self, device=None) -> "State":
         dev = device or self.w_flat.device
