@@ -329,6 +329,9 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   if (ce != cudaSuccess) return cuda_fail(ce, "reading the step result");
   ce = cudaStreamSynchronize(h->stream);
   if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the step");
+  if (h->scalars_host->error)
+    return fail(LAMB_ERR_CUDA, "a bounded wait on the GPU gave up (staged copies did not "
+                               "arrive); the state of this step is undefined");
   out->skipped = h->scalars_host->skip;
   out->grad_norm = h->scalars_host->grad_norm;
   out->loss_scale = h->scalars_host->scale_used;

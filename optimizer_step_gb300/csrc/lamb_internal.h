@@ -63,7 +63,7 @@ struct StepScalars {
   float scale_used;    // S of this step
   float scale;         // dynamic loss scale for the next step
   int32_t good_steps;  // clean steps in a row since the last growth/backoff
-  int32_t pad;
+  int32_t error;       // set on the GPU if a bounded wait gave up this step
 };
 
 // How the grad-norm kernel finds this step's loss scale.
