@@ -78,6 +78,13 @@ namespace {
 #ifndef LAMB_DYNAMIC_BC
 #define LAMB_DYNAMIC_BC 1
 #endif
+// 1: the apply kernel walks the work table from its end.  It then starts on
+// the items the moments kernel finished last, whose m, v and w are still in
+// L2, and ends on the first items, which the next step's moments kernel
+// takes first.  Elements are independent, so results do not depend on it.
+#ifndef LAMB_REVERSE_C
+#define LAMB_REVERSE_C 1
+#endif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
@@ -571,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTa
   __shared__ int32_t slot;
   ItemQueue q{&T.queue[1], T.n_items, &slot, int32_t(blockIdx.x)};
   for (int32_t it = q.next(); it < T.n_items; it = q.next()) {
-    const lamb_work_item wi = T.items[it];
+    const lamb_work_item wi = T.items[LAMB_REVERSE_C ? T.n_items - 1 - it : it];
     if (wi.tensor < 0) continue;  // packs were finished by the moments kernel
     const TensorDesc d = T.td[wi.tensor];
     const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
@@ -656,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_tma_kernel(D
   bool ok = true;
   ItemQueue q{&T.queue[1], T.n_items, &slot, int32_t(blockIdx.x)};
   for (int32_t it = q.next(); it < T.n_items && ok; it = q.next()) {
-    const lamb_work_item wi = T.items[it];
+    const lamb_work_item wi = T.items[LAMB_REVERSE_C ? T.n_items - 1 - it : it];
     if (wi.tensor < 0) continue;
     const TensorDesc d = T.td[wi.tensor];
     const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
