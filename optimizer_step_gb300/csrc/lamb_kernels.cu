@@ -29,8 +29,10 @@
 // tensors; packs of small tensors, a warp per tensor).  Grids are persistent
 // (a few CTAs per SM): the grad-norm kernel's CTAs walk items blockIdx.x,
 // blockIdx.x + gridDim.x, ...; the moments and apply kernels take items
-// greedily from an atomic counter, which balanced better on GB300.  Every
-// reduction has a fixed order, so results are deterministic run to run.
+// greedily from an atomic counter, which balanced better on GB300, the
+// moments kernel from the table's start and the apply kernel from its end (so
+// each starts where the other left data in L2).  Every reduction has a fixed
+// order, so results are deterministic run to run.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
