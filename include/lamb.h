@@ -171,6 +171,12 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
  * device slots, so alternating among up to four grad buffers costs no upload;
  * a new set is written by a small kernel, never by a copy (a copy could queue
  * behind unrelated bulk transfers on the copy engine).
+ *
+ * Errors: LAMB_ERR_INVALID and LAMB_ERR_ALIGN are found before anything is
+ * enqueued, and the state is untouched.  LAMB_ERR_CUDA means that a launch, a
+ * copy or the wait failed, or that a bounded wait inside the apply kernel
+ * gave up (its staged copies from HBM never arrived); the state may then be
+ * partly updated and should be restored from a snapshot.
  */
 LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
                        float loss_scale, lamb_result* out);
