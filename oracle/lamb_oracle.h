@@ -40,7 +40,10 @@
  * with dyadic betas, pure weight decay, zero-weight and zero-direction
  * tensors, scale invariance of the trust ratio, bit-exact power-of-two loss
  * scaling, clip equivalences, per-tensor independence, inf/NaN skip, and the
- * bf16/fp16 conversions against library routines.
+ * bf16/fp16 conversions against library routines.  The t=1 closed form, the
+ * grad norm under active clipping, the power-of-two loss scale and the
+ * inf/NaN skip are pinned again on tensors of more than one 65,536-element
+ * block (the block-by-block path), with weight-decay flags mixed.
  */
 #ifndef LAMB_ORACLE_H
 #define LAMB_ORACLE_H

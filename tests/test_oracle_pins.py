@@ -410,3 +410,104 @@ def test_loss_scale_growth_never_overflows():
     s, g = 3.0e38, 0
     s, g = oracle.loss_scale_update(s, g, 0, growth=2.0, backoff=0.5, growth_interval=1)
     assert s == np.float32(3.0e38) and g == 0
+
+
+# ------------------------------------- tensors of more than one block
+# The oracle walks tensors of more than 65,536 elements block by block (one
+# block of direction values per thread, block partials of the norms added in
+# block order).  These pins repeat the closed forms on tensors that take that
+# path -- one element past a block, several full blocks plus a ragged tail --
+# with weight-decay flags mixed, so that a partial sum dropped, a block's r
+# applied at the wrong offset or a flag ignored there fails a pin.
+BIG = [65537, 200003, 3 * 65536 + 5, 300]
+BIG_WD = [1, 0, 1, 0]
+
+
+def decoded(bits, grad_dtype):
+    """bf16 / fp16 bit patterns -> float64 with numpy and torch (not the oracle)."""
+    if grad_dtype == oracle.GRAD_FP16:
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_multi_block_first_step_closed_form():
+    """t=1, m=v=0, eps=0: r = sign(g) + wd*w, trust = ||w||/||r||, w' = w - lr*trust*r,
+    element by element over every block of every tensor."""
+    rng = np.random.default_rng(21)
+    st = rand_state(rng, BIG)
+    w0 = [a.astype(np.float64) for a in st[0]]
+    ghat = [decoded(g, oracle.GRAD_BF16) for g in st[4]]
+    assert all(np.all(x != 0) for x in ghat)
+    wd, lr = 0.25, 0.01
+    sk, gn, trust = run(st, BIG_WD, eps=0.0, weight_decay=wd, lr=lr)
+    assert sk == 0
+    assert close(gn, np.linalg.norm(np.concatenate(ghat)), 1e-13)
+    for i, flag in enumerate(BIG_WD):
+        r = np.sign(ghat[i]) + flag * wd * w0[i]
+        tr = np.linalg.norm(w0[i]) / np.linalg.norm(r)
+        assert close(trust[i], tr, 1e-12), (i, trust[i], tr)
+        assert close(st[0][i], w0[i] - lr * tr * r, 1.2e-7, floor=1e-30), i
+        assert close(st[1][i], (1 - float(B1)) * ghat[i], 1.2e-7, floor=1e-30), i
+        assert close(st[2][i], (1 - float(B2)) * ghat[i] ** 2, 1.2e-7, floor=1e-30), i
+        assert np.array_equal(st[3][i], bf16_bits_of(st[0][i])), i
+
+
+@pytest.mark.parametrize("grad_dtype", [oracle.GRAD_BF16, oracle.GRAD_FP16])
+def test_multi_block_grad_norm_and_active_clip(grad_dtype):
+    """G = ||g/S|| over all blocks of all tensors (numpy), and the clip factor
+    clip/G reaches every block: m' = (1-b1)*(clip/G)*g^ at t=1."""
+    rng = np.random.default_rng(22)
+    S = 256.0
+    st = rand_state(rng, BIG, grad_dtype)
+    st[4][:] = [to_bits(rng.normal(0, 1e-3, n) * S, grad_dtype) for n in BIG]
+    ghat = [decoded(g, grad_dtype) / S for g in st[4]]
+    G = np.linalg.norm(np.concatenate(ghat))
+    clip = 0.3 * G
+    w0 = [a.astype(np.float64) for a in st[0]]
+    lr = 0.02
+    sk, gn, trust = run(st, BIG_WD, eps=0.0, weight_decay=0.0, lr=lr, clip=clip,
+                        loss_scale=S, grad_dtype=grad_dtype)
+    assert sk == 0
+    assert close(gn, G, 1e-13)
+    c = clip / G
+    for i, n in enumerate(BIG):
+        assert close(st[1][i], (1 - float(B1)) * c * ghat[i], 1.2e-7, floor=1e-30), i
+        assert close(st[2][i], (1 - float(B2)) * (c * ghat[i]) ** 2, 1.2e-7, floor=1e-30), i
+        tr = np.linalg.norm(w0[i]) / math.sqrt(n)  # r = sign(c g) = sign(g)
+        assert close(trust[i], tr, 1e-12), i
+        assert close(st[0][i], w0[i] - lr * tr * np.sign(ghat[i]), 1.2e-7, floor=1e-30), i
+
+
+@pytest.mark.parametrize("k", [3, 12])
+def test_multi_block_power_of_two_loss_scale_is_bit_exact(k):
+    rng = np.random.default_rng(23 + k)
+    mags = [rng.uniform(-8, -1, n) for n in BIG]
+    signs = [rng.choice([-1.0, 1.0], n) for n in BIG]
+    g_true = [np.asarray(s * 2.0 ** e, np.float16) for s, e in zip(signs, mags)]
+    base = rand_state(rng, BIG, zero_mv=False)
+    a, b = copy_state(base), copy_state(base)
+    a[4][:] = [x.view(np.uint16).copy() for x in g_true]
+    b[4][:] = [(x.astype(np.float32) * np.float32(2.0 ** k)).astype(np.float16)
+               .view(np.uint16).copy() for x in g_true]
+    ra = run(a, BIG_WD, grad_dtype=oracle.GRAD_FP16, loss_scale=1.0, t=6, clip=0.5)
+    rb = run(b, BIG_WD, grad_dtype=oracle.GRAD_FP16, loss_scale=2.0 ** k, t=6, clip=0.5)
+    assert ra[0] == rb[0] == 0 and ra[1] == rb[1]
+    for la, lb in zip(a[:4], b[:4]):
+        for x, y in zip(la, lb):
+            assert x.tobytes() == y.tobytes()
+
+
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+def test_multi_block_nonfinite_anywhere_skips(where):
+    """An inf/NaN in any block of a multi-block tensor skips the whole step."""
+    rng = np.random.default_rng(24)
+    st = rand_state(rng, BIG, zero_mv=False)
+    n = BIG[1]
+    idx = {"first": 0, "middle": 2 * 65536 + 17, "last": n - 1}[where]
+    st[4][1][idx] = 0x7FC0 if where == "middle" else 0x7F80
+    before = copy_state(st)
+    sk, gn, _ = run(st, BIG_WD, t=3, clip=1.0)
+    assert sk == 1 and gn == math.inf
+    for la, lb in zip(st, before):
+        for x, y in zip(la, lb):
+            assert x.tobytes() == y.tobytes()
