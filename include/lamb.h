@@ -8,12 +8,13 @@
  * Deep Learning: Training BERT in 76 minutes", ICLR 2020) is Adam with a
  * per-tensor ("layer-wise") trust ratio.  MegaScale adopts it so the batch can
  * grow 4x without losing accuracy ("MegaScale: Scaling Large Language Model
- * Training to More Than 10,000 GPUs", guided-reading digest, section 2: LAMB
- * adapts the learning rate per layer; the same digest's section 8, Table 3,
- * credits it with +3.0 MFU points).  The state it updates is the rank's ZeRO-2
- * shard (digest section 3, "Data parallelism (ZeRO-2 style)", and the "Terms"
- * entry for ZeRO-2: optimizer state and gradients sharded over the
- * data-parallel ranks).  For tensor i with n_i elements, at step t:
+ * Training to More Than 10,000 GPUs", guided-reading digest, section 2: the
+ * step size is scaled tensor by tensor through a trust ratio; the same
+ * digest's section 8, Table 3, credits it with +3.0 MFU points).  The state
+ * it updates is the rank's ZeRO-2 shard (digest section 3, "Data parallelism
+ * (ZeRO-2 style)", and the "Terms" entry for ZeRO-2: optimizer state and
+ * gradients sharded over the data-parallel ranks).  For tensor i with n_i
+ * elements, at step t:
  *
  *   per element   g' = c * g / S                       (S: loss scale)
  *                 m  = b1 m + (1 - b1) g'
@@ -305,15 +306,24 @@ LAMB_API void lamb_plan_limits(int64_t* chunk_elems, int64_t* min_chunk_elems,
  *
  * It allocates nothing: no cudaMalloc, no cudaFree, no pinned memory.  Its
  * scratch (tensor table, per-CTA partial sums, completion ticket) is one
- * fixed device array of LAMB_NOALLOC_SCRATCH_BYTES inside this library, which
- * every GPU that loads the library holds until the process exits.  The first
- * call on each device looks up that array's device address and sizes the
- * grid (with the device current); make that first call before any stream
- * capture.  Every call reuses the same array and clears its ticket and flag
- * first, so calls whose work overlaps on the GPU (on different streams or
- * host threads without ordering between them) race and give wrong results;
- * calls in one stream are ordered and safe.  The call returns once the work
- * is enqueued.
+ * fixed device array of LAMB_NOALLOC_SCRATCH_BYTES inside this library.  The
+ * tensor table is written by small kernels whose launch arguments carry the
+ * entries, so nothing is read from host memory after the call returns.
+ *
+ * First call on each device.  It looks up that array's device address, sizes
+ * the grid and loads this entry point's kernels, with the device current.
+ * Under CUDA's lazy module loading (the default) that first call is also
+ * when the array and the kernels' code are placed in the device's memory, and
+ * they stay there until the process exits; it can therefore fail for lack of
+ * memory.  A caller that needs this entry point when memory is exhausted
+ * (for example an out-of-memory recovery path) should make one call at
+ * start-up, while memory is free (n_tensors = 0 is enough), and make that
+ * first call before any stream capture.  Later calls take no device memory.
+ *
+ * Every call reuses the same array and clears its ticket and flag first, so
+ * calls whose work overlaps on the GPU (on different streams or host threads
+ * without ordering between them) race and give wrong results; calls in one
+ * stream are ordered and safe.  The call returns once the work is enqueued.
  */
 #define LAMB_NOALLOC_MAX_TENSORS 8192
 #define LAMB_NOALLOC_SCRATCH_BYTES (256 + 1024 * 8 + LAMB_NOALLOC_MAX_TENSORS * 16)

@@ -166,6 +166,29 @@ __global__ void __launch_bounds__(kNaThreads) grad_norm_noalloc_kernel(unsigned 
   }
 }
 
+// Writes entries [at, at + count) of the tensor table into the scratch array
+// from the kernel's own arguments (kNaTablePerLaunch entries, 3840 bytes, under
+// the 4 KB parameter limit), and the first launch of a call clears the ticket
+// and the inf/NaN flag.  Each launch carries its entries by value, so a call
+// never reads host memory after it returns.
+constexpr int kNaTablePerLaunch = 240;
+
+struct NaTableChunk {
+  NaTensor e[kNaTablePerLaunch];
+};
+
+__global__ void noalloc_table_kernel(unsigned char* scratch, int32_t at, int32_t count,
+                                     int32_t clear_header, NaTableChunk chunk) {
+  NaTensor* tab = reinterpret_cast<NaTensor*>(scratch + kHeaderBytes + kPartialBytes);
+  const int i = threadIdx.x;
+  if (i < count) tab[at + i] = chunk.e[i];
+  if (clear_header && i == 0) {
+    NaHeader* hd = reinterpret_cast<NaHeader*>(scratch);
+    hd->ticket = 0u;
+    hd->nonfinite = 0u;
+  }
+}
+
 int na_fail(int code, const std::string& msg) {
   lambgb::set_last_error(msg);
   return code;
@@ -175,7 +198,6 @@ int na_fail(int code, const std::string& msg) {
 std::mutex na_mutex;
 void* na_scratch_addr[kNaMaxDevices] = {};
 int na_grid[kNaMaxDevices] = {};
-NaTensor na_host_table[LAMB_NOALLOC_MAX_TENSORS];  // staging for the upload, under na_mutex
 
 }  // namespace
 
@@ -231,26 +253,44 @@ LAMB_API int lamb_grad_norm_noalloc(int32_t n_tensors, const int64_t* sizes,
           &per_sm, grad_norm_noalloc_kernel<LAMB_GRAD_BF16>, kNaThreads, 0);
     if (ce != cudaSuccess || sms <= 0 || per_sm <= 0)
       return na_fail(LAMB_ERR_CUDA, "occupancy query failed");
+    // Load the other kernels now too (lazy module loading would otherwise
+    // load each one, and take device memory for its code, at its first use).
+    cudaFuncAttributes fa;
+    ce = cudaFuncGetAttributes(&fa, grad_norm_noalloc_kernel<LAMB_GRAD_FP16>);
+    if (ce == cudaSuccess) ce = cudaFuncGetAttributes(&fa, noalloc_table_kernel);
+    if (ce != cudaSuccess)
+      return na_fail(LAMB_ERR_CUDA, std::string("loading the kernels: ") +
+                                        cudaGetErrorString(ce));
     na_grid[dev] = sms * per_sm < kNaMaxCtas ? sms * per_sm : kNaMaxCtas;
     na_scratch_addr[dev] = p;
   }
   unsigned char* scratch = static_cast<unsigned char*>(na_scratch_addr[dev]);
 
-  // Upload the tensor table (stream-ordered after any earlier call on this
-  // stream) and clear the ticket and the inf/NaN flag.
+  // Write the tensor table (empty tensors left out) and clear the ticket and
+  // the inf/NaN flag, stream-ordered after any earlier call on this stream.
   int32_t used = 0;
-  for (int32_t i = 0; i < n_tensors; ++i) {
+  NaTableChunk chunk;
+  int count = 0;
+  bool first = true;
+  auto flush = [&]() {
+    noalloc_table_kernel<<<1, kNaTablePerLaunch, 0, s>>>(scratch, used - count, count,
+                                                         first ? 1 : 0, chunk);
+    first = false;
+    count = 0;
+    return cudaGetLastError();
+  };
+  ce = cudaSuccess;
+  for (int32_t i = 0; i < n_tensors && ce == cudaSuccess; ++i) {
     if (sizes[i] == 0) continue;
-    na_host_table[used].g = static_cast<const uint16_t*>(grads[i]);
-    na_host_table[used].n = sizes[i];
+    chunk.e[count].g = static_cast<const uint16_t*>(grads[i]);
+    chunk.e[count].n = sizes[i];
+    ++count;
     ++used;
+    if (count == kNaTablePerLaunch) ce = flush();
   }
-  ce = cudaMemsetAsync(scratch, 0, kHeaderBytes, s);
-  if (ce == cudaSuccess && used > 0)
-    ce = cudaMemcpyAsync(scratch + kHeaderBytes + kPartialBytes, na_host_table,
-                         size_t(used) * sizeof(NaTensor), cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess && (count > 0 || first)) ce = flush();
   if (ce != cudaSuccess)
-    return na_fail(LAMB_ERR_CUDA, std::string("staging the tensor table: ") +
+    return na_fail(LAMB_ERR_CUDA, std::string("writing the tensor table: ") +
                                       cudaGetErrorString(ce));
   if (grad_dtype == LAMB_GRAD_FP16)
     grad_norm_noalloc_kernel<LAMB_GRAD_FP16><<<na_grid[dev], kNaThreads, 0, s>>>(

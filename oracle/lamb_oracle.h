@@ -13,7 +13,7 @@
  *   Training BERT in 76 minutes" (ICLR 2020), the layer-wise adaptive Adam
  *   update -- as adopted by MegaScale ("MegaScale: Scaling Large Language Model
  *   Training to More Than 10,000 GPUs", guided-reading digest, section 2: the
- *   learning rate is adapted per layer, which is what lets the batch grow 4x).
+ *   step size is scaled layer by layer, which is what lets the batch grow 4x).
  *   The step runs on one data-parallel rank's ZeRO-2 shard of optimizer state
  *   (same digest, section 3 "Data parallelism (ZeRO-2 style)" and the "Terms"
  *   entry for ZeRO-2): every tensor the rank owns is updated locally.

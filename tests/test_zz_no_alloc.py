@@ -3,10 +3,13 @@
 It is for callers that cannot allocate device memory at the moment they need
 the grad check (a framework allocator that has reserved nearly all of HBM, an
 out-of-memory recovery path).  These tests call it through the C ABI and
-compare what it writes with the grad norm, skip flag and clip factor that the
-full step (lamb_step) reports for the same grads, twice in a row, since every
-call reuses the same fixed scratch array.  The first call in this file also
-exercises the per-device set-up when the file runs alone in a fresh process.
+compare what it writes with the CPU oracle's grad norm and with the grad
+norm, skip flag and clip factor that the full step (lamb_step) reports for
+the same grads, twice in a row, since every call reuses the same fixed
+scratch array.  They also check that, after one warm-up call, further calls
+leave the device's free memory and torch's reserved memory unchanged.  The
+first call in this file also exercises the per-device set-up when the file
+runs alone in a fresh process.
 """
 import ctypes
 import math
@@ -15,12 +18,17 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from optimizer_step_gb300 import Lamb, _lib
 
 pytestmark = pytest.mark.gpu
 
 RTOL = 1e-5  # the one-step tolerance of the parity tests
+
+
+def f32c(x):
+    return float(np.float32(x))
 
 
 def _noalloc(lib, sizes, grads, grad_dtype, loss_scale, clip, out):
@@ -38,6 +46,21 @@ def _case(sizes, grad_dtype, S, clip, inject=None, seed=11):
                     grad_dtype, t0=5, lr=1e-3, clip=clip, loss_scale=S, warm_state=True,
                     grad_kind="normal", grad_sigma=1e-3, seed=seed, inject=dict(inject or {}))
     return wl
+
+
+def _oracle_grad_norm(wl, gv):
+    """The oracle's grad norm and skip flag for these grads (no state updated)."""
+    g_host = [W.as_bits(x) for x in gv]
+    n = len(g_host)
+    none = [None] * n
+    f32 = lambda x: float(np.float32(x))
+    gd = oracle.GRAD_FP16 if wl.grad_dtype == torch.float16 else oracle.GRAD_BF16
+    sk, gn = oracle.lamb_step(none, none, none, none, g_host, wl.wd_flags, grad_dtype=gd,
+                              beta1=f32(wl.beta1), beta2=f32(wl.beta2), eps=f32(wl.eps),
+                              weight_decay=f32(wl.weight_decay), lr=f32(wl.lr), t=wl.t0,
+                              clip=f32(wl.clip), loss_scale=f32(wl.loss_scale),
+                              update_mask=[0] * n)
+    return sk, gn
 
 
 def _reference(wl, gv):
@@ -61,12 +84,15 @@ def test_noalloc_grad_norm_matches_lamb_step_on_two_calls(grad_dtype, S, clip):
         assert _noalloc(lib, sizes, gv, code, S, clip, out) == 0, lib.lamb_last_error()
         torch.cuda.synchronize()
         outs.append(out.tolist())
+    osk, ogn = _oracle_grad_norm(wl, gv)
     skipped, gn = _reference(wl, gv)
-    assert skipped is False
+    assert skipped is False and osk == 0
+    assert abs(gn - ogn) <= RTOL * ogn
     for gn_na, c_na, nf_na in outs:
         assert nf_na == 0.0
-        assert abs(gn_na - gn) <= RTOL * gn
-        c_ref = clip / gn if (clip > 0 and gn > clip) else 1.0
+        assert abs(gn_na - ogn) <= RTOL * ogn  # against the oracle
+        assert abs(gn_na - gn) <= RTOL * gn    # against lamb_step
+        c_ref = f32c(clip) / ogn if (clip > 0 and ogn > f32c(clip)) else 1.0
         assert abs(c_na - c_ref) <= RTOL * c_ref
     assert outs[0] == outs[1]  # same grads, same fixed reduction order
 
@@ -84,6 +110,7 @@ def test_noalloc_flags_nonfinite_like_lamb_step_on_two_calls():
         assert nf_na == 1.0 and gn_na == math.inf and c_na == 0.0
     skipped, gn = _reference(wl, gv)
     assert skipped is True and gn == math.inf
+    assert _oracle_grad_norm(wl, gv) == (1, math.inf)
     # A clean call afterwards starts from a cleared flag.
     _, gv2 = W.make_grads(wl, 2, "cuda")
     out = torch.zeros(3, dtype=torch.float64, device="cuda")
@@ -102,3 +129,34 @@ def test_noalloc_rejects_more_tensors_than_its_scratch_holds():
                                     ctypes.c_void_p(out.data_ptr()), None)
     assert rc == _lib.LAMB_ERR_INVALID
     assert b"LAMB_NOALLOC_MAX_TENSORS" in lib.lamb_last_error()
+
+
+def test_noalloc_calls_take_no_device_memory_after_a_warm_up_call():
+    """After one warm-up call (which may load the library's module and its
+    fixed array), ten more calls with both grad types leave the free device
+    memory and torch's reserved memory exactly as they were."""
+    lib = _lib.load()
+    sizes = [300, 4097, 70001, 1 << 18]
+    gvs = []
+    for dt in (torch.bfloat16, torch.float16):
+        _, gv = W.make_grads(_case(sizes, dt, 1.0, 0.0), 1, "cuda")
+        gvs.append((dt, gv))
+    out = torch.zeros(3, dtype=torch.float64, device="cuda")
+    warm = torch.zeros(3, dtype=torch.float64, device="cuda")
+    assert _noalloc(lib, [], [], _lib.LAMB_GRAD_BF16, 1.0, 0.0, warm) == 0, lib.lamb_last_error()
+    torch.cuda.synchronize()
+    assert warm.tolist() == [0.0, 1.0, 0.0]  # empty input: norm 0, no clip, finite
+    torch.cuda.mem_get_info()  # the query itself sets nothing up after this
+    free0 = torch.cuda.mem_get_info()[0]
+    reserved0 = torch.cuda.memory_reserved()
+    results = []
+    for k in range(10):
+        dt, gv = gvs[k % 2]
+        code = _lib.LAMB_GRAD_FP16 if dt == torch.float16 else _lib.LAMB_GRAD_BF16
+        assert _noalloc(lib, sizes, gv, code, 1.0, 0.0, out) == 0, lib.lamb_last_error()
+        torch.cuda.synchronize()
+        results.append(out[0].item())
+        assert torch.cuda.mem_get_info()[0] == free0, f"call {k} changed free device memory"
+        assert torch.cuda.memory_reserved() == reserved0
+    assert all(math.isfinite(x) and x > 0 for x in results)
+    assert results[0] == results[2] and results[1] == results[3]
