@@ -3,8 +3,9 @@
 
 Default workload: one GPT-175B-shaped parallel block as a ZeRO-2 shard
 (d=12288, ffn=49152; 1,811,963,904 fp32 params, bf16 grads, t=1000, global
-clip 1.0).  A step is one call of the library's ``lamb_step`` (grad-norm,
-moments and apply kernels, plus the result readback).
+clip 1.0).  A step is one call of the library's ``lamb_step_async``: the
+grad-norm, moments and apply kernels, with the step's outcome written by the
+GPU into pinned host memory; the host does not wait between steps.
 
 Prints one JSON line on rank 0:
   value      params/s over all ranks with every input resident in HBM
@@ -39,9 +40,10 @@ METRIC = "LAMB step params/s and achieved HBM GB/s (% of GB300 peak), 175B-layer
 UNIT = "params/s"
 # Algorithmic HBM bytes per parameter of each kernel (16-bit grads, fp32 w/m/v,
 # bf16 weight copy): grad norm reads g; moments reads g, m, v, w and writes m, v;
-# apply reads m, v, w and writes w and the bf16 copy.  Small tensors (packed,
-# at most small_max elements) are finished inside the moments kernel, which
-# then also writes their w and bf16 copy (28 B) while apply skips them.
+# apply reads m, v, w and writes w and the bf16 copy.  Tensors the moments
+# kernel finishes in one pass (packed small tensors, and tensors of a single
+# work item) have it also write their w and bf16 copy (28 B) while apply skips
+# them.
 BYTES_PER_PARAM = {"grad_norm": 2, "moments": 22, "apply": 18}
 PACKED_BYTES_PER_PARAM = {"grad_norm": 2, "moments": 28, "apply": 0}
 
@@ -52,11 +54,8 @@ def kernel_bytes(n_params: int, n_packed: int) -> dict:
             for k in BYTES_PER_PARAM}
 
 
-def packed_params(sizes) -> int:
-    from optimizer_step_gb300 import plan_limits
-    small = plan_limits()["small_max"]
-    return int(sum(n for n in sizes if 0 < n <= small))
 FLOOR_BYTES_PER_PARAM = 28  # g read + w/m/v read and write + bf16 write
+RESULT_RECORD_BYTES = 40    # one step's outcome, written by the GPU into pinned host memory
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCE = os.path.join(ROOT, "optimizer_step_gb300", "csrc", "lamb_kernels.cu")
@@ -82,7 +81,8 @@ def parse_args(argv=None):
                         "stage of a checkpoint) and a step issued while it runs")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="CPU oracle budget for the cpu_baseline sample")
+                   help="time budget of the cpu_baseline's timed oracle steps (at least one "
+                        "step runs; the reference arm takes ten times this)")
     return p.parse_args(argv)
 
 
@@ -223,44 +223,44 @@ def traffic_per_launch(kernel: str, n_params: int):
 
 
 # ----------------------------------------------------------- CPU baseline
-def cpu_sample(wl, max_elems: int):
+def host_state_from(st, gflat, wl):
+    """Host (numpy) per-tensor views of a state and a grad buffer."""
     import workloads as W
-    return W.scaled(wl, max_elems)
+    flat = [st.w_flat.cpu().numpy(), st.m_flat.cpu().numpy(), st.v_flat.cpu().numpy(),
+            W.as_bits(st.w16_flat)]
+    g = W.as_bits(gflat)
+    views = lambda a: [a[o:o + n] for o, n in zip(st.offsets, wl.sizes)]
+    return [views(a) for a in flat], views(g)
 
 
-def time_oracle(wl, steps: int, warmup: int, budget_s: float, max_elems: int):
-    """Times the CPU oracle on a scaled sample of the workload.  Returns
-    (params/s, sample description, threads, steps run, seconds)."""
+def time_oracle(wl, host, g, steps: int, warmup: int, budget_s: float):
+    """Times the CPU oracle, as it stands, on the whole workload (every tensor
+    at full size): ``warmup`` untimed steps, then timed steps until ``steps``
+    are done or ``budget_s`` has passed (at least one).  Returns (params/s,
+    sample description, threads, steps timed, seconds)."""
     import numpy as np
     import torch
 
     import oracle
-    import workloads as W
-    sw = cpu_sample(wl, max_elems)
-    st = W.make_state(sw, "cpu")
-    host = [[x.numpy() for x in st.w], [x.numpy() for x in st.m], [x.numpy() for x in st.v],
-            [W.as_bits(x).copy() for x in st.w16]]
-    _, gv = W.make_grads(sw, 1, "cpu")
-    g = [W.as_bits(x).copy() for x in gv]
-    gd = oracle.GRAD_FP16 if sw.grad_dtype == torch.float16 else oracle.GRAD_BF16
+    gd = oracle.GRAD_FP16 if wl.grad_dtype == torch.float16 else oracle.GRAD_BF16
     f32 = lambda x: float(np.float32(x))
-    kw = dict(grad_dtype=gd, beta1=f32(sw.beta1), beta2=f32(sw.beta2), eps=f32(sw.eps),
-              weight_decay=f32(sw.weight_decay), lr=f32(sw.lr), clip=f32(sw.clip),
-              loss_scale=f32(sw.loss_scale))
-    t = sw.t0
+    kw = dict(grad_dtype=gd, beta1=f32(wl.beta1), beta2=f32(wl.beta2), eps=f32(wl.eps),
+              weight_decay=f32(wl.weight_decay), lr=f32(wl.lr), clip=f32(wl.clip),
+              loss_scale=f32(wl.loss_scale))
+    t = wl.t0
     for _ in range(warmup):
-        oracle.lamb_step(*host, g, sw.wd_flags, t=t, **kw)
+        oracle.lamb_step(*host, g, wl.wd_flags, t=t, **kw)
         t += 1
     done, t0 = 0, time.perf_counter()
     while done < steps and (done == 0 or time.perf_counter() - t0 < budget_s):
-        oracle.lamb_step(*host, g, sw.wd_flags, t=t, **kw)
+        oracle.lamb_step(*host, g, wl.wd_flags, t=t, **kw)
         t += 1
         done += 1
     el = time.perf_counter() - t0
     threads = os.cpu_count() or 1
-    desc = (f"{sw.n_params:,} params: every tensor of the workload cut to at most {max_elems:,} "
-            f"elements ({len(sw.sizes)} tensors), {done} timed oracle steps")
-    return sw.n_params * done / el, desc, threads, done, el
+    desc = (f"the whole workload: {wl.n_params:,} params in {len(wl.sizes)} tensors at full "
+            f"size, {warmup} untimed and {done} timed oracle steps on {threads} host threads")
+    return wl.n_params * done / el, desc, threads, done, el
 
 
 # ---------------------------------------------------------------- our arm
@@ -283,44 +283,58 @@ def run_ours(args, world, rank, local):
     gflat, gv = W.make_grads(wl, 1, device)
     opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, beta1=wl.beta1, beta2=wl.beta2,
                eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype)
-    opt.set_grads(gv)
-    opt.set_timing(True)
+    grads0 = opt.prepare_grads(gv)
+    opt.set_grads(grads0)
     if args.dynamic_loss_scale:
         opt.set_loss_scaler(init_scale=wl.loss_scale, growth_interval=2000)
     stream = opt.stream
-    t = wl.t0
+    # Asynchronous steps: the step number lives on the GPU and advances only
+    # on steps that are not skipped; nothing waits for the GPU between steps.
+    opt.set_step(wl.t0)
 
     def step():
-        nonlocal t
-        sk, _ = opt.step(wl.lr, t, wl.clip, wl.loss_scale)
-        if not sk:
-            t += 1
-        return sk
+        return opt.step_async(wl.lr, wl.clip, wl.loss_scale)
 
     for _ in range(max(3, args.warmup)):
-        step()
+        seq = step()
+    opt.result(seq)
     torch.cuda.synchronize()
     barrier(world)
 
-    # ---- device-resident timed region
+    # ---- device-resident timed region: every step's outcome is written by
+    # the GPU into the handle's pinned result ring inside the region.  The
+    # library's event monitor is off here: events between the kernels would
+    # stop each kernel from launching while the one before it drains.
     sampler = ClockSampler(local)
     sampler.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ktimes = []
-    skips = 0
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.steps):
-        skips += int(step())
-        ktimes.append(opt.kernel_times())
+    seqs = [step() for _ in range(args.steps)]
     e1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     barrier(world)
     sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
     value = whole_job_rate(N, args.steps, world, sec)
+    kept = seqs[-64:]  # the library keeps the last 64 steps' outcomes
+    skips = sum(int(opt.result(q)[0]) for q in kept)
 
-    n_packed = packed_params(wl.sizes)
+    # ---- second timed region, the same steps with the event monitor on: the
+    # per-kernel durations (events before and after each kernel, on the
+    # handle's stream) for the roofline.
+    opt.set_timing(True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    seqs = [step() for _ in range(args.steps)]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    monitored_ms = e0.elapsed_time(e1) / args.steps
+    ktimes = [opt.kernel_times(q) for q in seqs[-64:]]
+    skips += sum(int(opt.result(q)[0]) for q in seqs[-64:])
+    opt.set_timing(False)
+
+    n_packed = opt.one_pass_params()
     kbytes = kernel_bytes(N, n_packed)
     step_bytes = sum(kbytes.values())
     kern = {}
@@ -333,7 +347,9 @@ def run_ours(args, world, rank, local):
     step_ms = sec / args.steps * 1e3
     dominant = "moments"
     achieved = kern[dominant]["GB/s"]
-    traffic = traffic_per_launch(dominant, N) if n_packed == 0 else None
+    # The recorded counters come from a cut of the same tensor mix; they are
+    # scaled by params only while one-pass tensors are a negligible share.
+    traffic = traffic_per_launch(dominant, N) if n_packed < N // 1000 else None
 
     # ---- end to end: every step's grads come from pinned host memory.  Two
     # device grad buffers; the copy of step k+1 runs on a side stream while
@@ -343,9 +359,11 @@ def run_ours(args, world, rank, local):
     if not args.no_e2e:
         pinned = gflat.cpu().pin_memory()
         gflat2, gv2 = W.grad_buffer(wl, device)
-        bufs, views = (gflat, gflat2), (gv, gv2)
+        bufs = (gflat, gflat2)
+        sets = (grads0, opt.prepare_grads(gv2))
         copy_stream = torch.cuda.Stream(device=device)
         copied = (torch.cuda.Event(), torch.cuda.Event())
+        freed = (torch.cuda.Event(), torch.cuda.Event())
         torch.cuda.synchronize()
         barrier(world)
         e0.record(stream)
@@ -353,30 +371,38 @@ def run_ours(args, world, rank, local):
         with torch.cuda.stream(copy_stream):
             bufs[0].copy_(pinned, non_blocking=True)
             copied[0].record(copy_stream)
+        e2e_seqs = []
         for k in range(args.steps):
-            if k + 1 < args.steps:  # buffer (k+1)%2 is free: step k-1 has returned
+            if k + 1 < args.steps:
+                nb = (k + 1) % 2
+                if k >= 1:  # step k-1 read buffer nb: the copy waits for it on the GPU
+                    copy_stream.wait_event(freed[nb])
                 with torch.cuda.stream(copy_stream):
-                    bufs[(k + 1) % 2].copy_(pinned, non_blocking=True)
-                    copied[(k + 1) % 2].record(copy_stream)
+                    bufs[nb].copy_(pinned, non_blocking=True)
+                    copied[nb].record(copy_stream)
             stream.wait_event(copied[k % 2])
-            opt.set_grads(views[k % 2])
-            step()
+            opt.set_grads(sets[k % 2])
+            e2e_seqs.append(step())
+            freed[k % 2].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         sec_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+        e2e_skips = sum(int(opt.result(q)[0]) for q in e2e_seqs[-64:])
         e2e = {"value": whole_job_rate(N, args.steps, world, sec_e2e), "unit": UNIT,
                "h2d_bytes_per_step": int(gflat.numel() * gflat.element_size()),
-               "d2h_bytes_per_step": 24, "ms_per_step": round(sec_e2e / args.steps * 1e3, 3),
-               "pipeline": "double-buffered grads; H2D of step k+1 overlaps step k"}
-        del pinned, gflat2, gv2, bufs, views
+               "d2h_bytes_per_step": RESULT_RECORD_BYTES,
+               "ms_per_step": round(sec_e2e / args.steps * 1e3, 3), "skipped_steps": e2e_skips,
+               "pipeline": "double-buffered grads; H2D of step k+1 overlaps step k; every "
+                           "step's outcome written by the GPU into pinned host memory"}
+        del pinned, gflat2, gv2, bufs, sets
 
     # ---- state snapshot into pinned host memory (checkpoint stage 1)
     snap = None
     if args.snapshot:
         host = [[torch.empty(n, dtype=torch.float32, pin_memory=True) for n in wl.sizes]
                 for _ in range(3)]
-        opt.set_grads(gv)
+        opt.set_grads(grads0)
         torch.cuda.synchronize()
         for _ in range(2):  # the first pass also maps the fresh pinned pages
             t0 = time.perf_counter()
@@ -385,7 +411,7 @@ def run_ours(args, world, rank, local):
             alone = time.perf_counter() - t0
         t0 = time.perf_counter()
         opt.snapshot_async(*host)
-        step()                      # its state-writing kernels wait on the GPU
+        opt.result(step())          # its state-writing kernels wait on the GPU
         opt.snapshot_wait()
         both = time.perf_counter() - t0
         nbytes = 12 * N
@@ -396,11 +422,17 @@ def run_ours(args, world, rank, local):
         del host
 
     opt.close()
-    del st, gflat, gv
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, threads, _, _ = time_oracle(wl, 1000, 1, args.cpu_seconds, 1 << 22)
+        # The oracle on the host cores, on a host copy of this same workload.
+        host, g_host = host_state_from(st, gflat, wl)
+        del st, gflat, gv
+        torch.cuda.empty_cache()
+        rate, desc, threads, _, _ = time_oracle(wl, host, g_host, 1000, 1, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        del host, g_host
+    else:
+        del st, gflat, gv
 
     if rank == 0:
         out = {
@@ -424,6 +456,7 @@ def run_ours(args, world, rank, local):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes": kbytes[dominant]},
             "kernels": kern,
+            "ms_per_step_monitored": round(monitored_ms, 4),
             "step_hbm": {"bytes_per_param": round(step_bytes / N, 4), "packed_params": n_packed,
                          "GB/s": round(step_bytes / (step_ms / 1e3) / 1e9, 1),
                          "frac_of_peak": round(step_bytes / (step_ms / 1e3) / 1e9 / peak, 4),
@@ -448,7 +481,14 @@ def run_reference(args, world, rank, local):
         return
     import workloads as W
     wl = W.WORKLOADS[args.config]()
-    rate, desc, threads, done, el = time_oracle(wl, args.steps, args.warmup, 1e9, 1 << 22)
+    if args.max_elems > 0:
+        wl = W.scaled(wl, args.max_elems)
+    st = W.make_state(wl, "cpu")
+    gflat, _ = W.make_grads(wl, 1, "cpu")
+    host, g_host = host_state_from(st, gflat, wl)
+    del st, gflat
+    rate, desc, threads, done, el = time_oracle(wl, host, g_host, args.steps,
+                                                args.warmup, args.cpu_seconds * 10)
     cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
     out = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
            "steps": done, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 3),

@@ -62,6 +62,7 @@ extern "C" {
 #define LAMB_ERR_ALIGN (-2)   /* a device pointer is not 16-byte aligned */
 #define LAMB_ERR_CUDA (-3)    /* a CUDA runtime call or a kernel launch failed */
 #define LAMB_ERR_NOMEM (-4)   /* device or pinned host allocation failed */
+#define LAMB_NOT_READY 1      /* lamb_step_result without waiting: not finished yet */
 
 /* Grad element types (all grads of one handle have the same type). */
 #define LAMB_GRAD_BF16 0
@@ -85,19 +86,21 @@ typedef struct {
 /* Outcome of one step.
  *   skipped          1 if some grad was inf or NaN; the step then wrote
  *                    nothing (w, m, v and w16 are bit-identical to before) and
- *                    the caller should not advance t; 0 otherwise
+ *                    the step number did not advance; 0 otherwise
  *   grad_norm        ||g / S|| over the whole shard, before clipping; +inf
  *                    when skipped
  *   loss_scale       the S this step divided the grads by
  *   next_loss_scale  the S the next step will use: with a dynamic loss scaler
  *                    (lamb_set_loss_scaler) the scale the next backward pass
- *                    must multiply the loss by; otherwise equal to loss_scale */
+ *                    must multiply the loss by; otherwise equal to loss_scale
+ *   t                the step number this step used for its bias corrections */
 typedef struct {
   int32_t skipped;
   int32_t reserved;
   double grad_norm;
   float loss_scale;
   float next_loss_scale;
+  int64_t t;
 } lamb_result;
 
 /* Dynamic loss scaling, kept on the GPU (see lamb_set_loss_scaler).
@@ -153,6 +156,79 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
                          void* stream);
 
 /*
+ * Create a handle over one rank's shard of a data-parallel (ZeRO-2) group
+ * whose shard boundaries may cut tensors.  ZeRO-2 gives each data-parallel
+ * rank a contiguous slice of the flattened optimizer state (MegaScale
+ * guided-reading digest, section 3, "Data parallelism (ZeRO-2 style)", and
+ * the "Terms" entry for ZeRO-2), so the first and the last tensor of a shard
+ * can be pieces of tensors that other ranks also hold.  LAMB's trust ratio
+ * needs ||w|| and ||r|| of the whole tensor, and the clip factor and the skip
+ * decision need the grad norm of the whole model, so such a group takes the
+ * step in three phases with two exchanges between them (the split step,
+ * lamb_split_norms / lamb_split_moments / lamb_split_apply below).
+ *
+ *   n_tensors ... w_bf16, hp, stream   as for lamb_create (the sizes are the
+ *                 local pieces' element counts)
+ *   exchange_slot  host array of n_tensors ints: -1 for a tensor this rank
+ *                 holds whole, or k in [0, n_slots) for a piece of a tensor
+ *                 shared with other ranks (each k given to at most one local
+ *                 tensor; the ranks sharing a tensor use the same k).  May be
+ *                 NULL when n_slots is 0.  Such tensors are never packed.
+ *   norm_exchange  device pointer to 2 doubles, caller-owned, 8-byte aligned:
+ *                 the grad-norm partials {sum of g^2 of the grads as given
+ *                 (before dividing by S), inf/NaN count}, written by
+ *                 lamb_split_norms, to be summed over the group in place
+ *   tensor_exchange  device pointer to 2 * n_slots doubles, caller-owned,
+ *                 8-byte aligned: {sum w^2, sum r^2} of slot k at [2k, 2k+1],
+ *                 written by lamb_split_moments (entries of slots this rank
+ *                 does not hold are left as they are: the caller zeroes them
+ *                 before summing), to be summed over the group in place
+ *
+ * A handle made by lamb_create has neither buffer and cannot take split
+ * steps; one made here takes ordinary steps too (a tensor with an exchange
+ * slot then gets its trust ratio from tensor_exchange as summed before the
+ * apply phase, so ordinary steps make sense only for a group of one rank).
+ */
+LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
+                                 const uint8_t* wd_flags, float* const* w, float* const* m,
+                                 float* const* v, uint16_t* const* w_bf16,
+                                 const int32_t* exchange_slot, int32_t n_slots,
+                                 double* norm_exchange, double* tensor_exchange,
+                                 const lamb_hparams* hp, void* stream);
+
+/*
+ * The split step, for a handle made by lamb_create_sharded.  Every call only
+ * enqueues work on the handle's stream; between the calls the caller sums the
+ * exchange buffers over the data-parallel group (for example with an
+ * all-reduce on the same stream, or through host memory after waiting for
+ * the stream), and every rank then continues with the same sums:
+ *
+ *   lamb_split_norms(h, grads, loss_scale)
+ *       reads this shard's grads and writes norm_exchange = {sum g^2, 0 or
+ *       1}.  loss_scale as for lamb_step (ignored while a dynamic loss scaler
+ *       is on).                              -> sum norm_exchange over the group
+ *   lamb_split_moments(h, lr, t, clip)
+ *       forms the grad norm ||g / S||, the clip factor and the skip decision
+ *       from the summed norm_exchange (a non-zero inf/NaN count skips the
+ *       step on every rank), then updates m and v, finishes every whole
+ *       tensor (its trust ratio; small whole tensors are also applied here)
+ *       and writes the {sum w^2, sum r^2} of each shared piece to its slot
+ *       of tensor_exchange.  t >= 1 fixes the step number; 0 takes the GPU's
+ *       counter (see lamb_step_async).          -> sum tensor_exchange over the group
+ *   lamb_split_apply(h, &seq)
+ *       forms the trust ratio of each shared tensor from its summed slot and
+ *       applies the update and the bf16 copy; seq (may be NULL) receives the
+ *       step's sequence number for lamb_step_result.
+ *
+ * The calls must come in this order (LAMB_ERR_INVALID otherwise, with nothing
+ * enqueued); no other step may start on the handle in between.  The result of
+ * a group of one rank, with no exchange at all, equals lamb_step's.
+ */
+LAMB_API int lamb_split_norms(lamb_handle* h, const void* const* grads, float loss_scale);
+LAMB_API int lamb_split_moments(lamb_handle* h, float lr, int64_t t, float clip);
+LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq);
+
+/*
  * One LAMB step.
  *
  *   grads       host array of n_tensors device pointers to this step's grads
@@ -181,6 +257,67 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
  */
 LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
                        float loss_scale, lamb_result* out);
+
+/*
+ * Asynchronous step: the same step as lamb_step, but the step number lives on
+ * the GPU and the call returns as soon as the work is enqueued, so the host
+ * never waits for the GPU between steps.
+ *
+ *   grads, lr, clip, loss_scale   as for lamb_step
+ *   seq         receives the step's sequence number (may be NULL), which
+ *               lamb_step_result takes
+ *
+ * The step number t is a counter on the GPU: the grad-norm kernel reads it,
+ * forms the bias corrections 1/(1 - beta1^t) and 1/(1 - beta2^t) in fp64, and
+ * advances it only if the step is not skipped, so the caller never has to
+ * learn the skip decision before enqueueing the next step.  A new handle's
+ * counter is 1; lamb_set_step sets it.  lamb_step (with an explicit t) also
+ * leaves the counter at t + 1 after a clean step and at t after a skipped
+ * one, so the two calls can be mixed.
+ *
+ * The outcome {skipped, grad_norm, loss_scale, next_loss_scale, t} is
+ * written by the GPU into a slot of a pinned, device-mapped ring owned by the
+ * handle; the last 64 steps' outcomes stay readable.  Grad buffers must stay
+ * valid and unchanged until the step has finished on the GPU (for example
+ * until the next work on the handle's stream that writes them).
+ *
+ * Errors: LAMB_ERR_INVALID and LAMB_ERR_ALIGN before anything is enqueued;
+ * LAMB_ERR_CUDA if a launch fails.  A bounded wait that gives up inside the
+ * apply kernel is reported by lamb_step_result for that step.
+ */
+LAMB_API int lamb_step_async(lamb_handle* h, const void* const* grads, float lr, float clip,
+                             float loss_scale, int64_t* seq);
+
+/*
+ * Outcome of a step enqueued by lamb_step_async (or lamb_step).
+ *
+ *   seq   the step's sequence number; one of the last 64 steps enqueued on
+ *         the handle (older ones: LAMB_ERR_INVALID, their slot was reused)
+ *   wait  != 0: block until the step has finished; 0: return LAMB_NOT_READY
+ *         (a positive value) at once if it has not
+ *   out   receives the outcome
+ *
+ * Returns LAMB_ERR_CUDA, with the state of that step undefined, if a bounded
+ * wait inside its apply kernel gave up.
+ */
+LAMB_API int lamb_step_result(lamb_handle* h, int64_t seq, int32_t wait, lamb_result* out);
+
+/* Number of elements the moments kernel finishes in one pass (packed small
+ * tensors and tensors of a single work item, unless shared with other ranks):
+ * their update re-reads the moments from cache, so they move 30 bytes per
+ * element over HBM instead of 42. */
+LAMB_API int lamb_one_pass_params(lamb_handle* h, int64_t* n);
+
+/* Sets the GPU's step counter (the t of the next lamb_step_async), t >= 1,
+ * in stream order on the handle's stream. */
+LAMB_API int lamb_set_step(lamb_handle* h, int64_t t);
+
+/* Device address of the dynamic loss scale (one fp32 on the handle's device,
+ * valid for the life of the handle): the scale the next step divides by while
+ * a dynamic loss scaler is on, updated by each step's grad-norm kernel.  A
+ * framework that never waits for lamb_step_result can read it on the GPU, in
+ * order on the handle's stream, to scale the next loss. */
+LAMB_API int lamb_loss_scale_device(lamb_handle* h, const float** scale);
 
 /*
  * Turn dynamic loss scaling on (cfg non-NULL) or off (NULL).  While it is on,
@@ -236,17 +373,21 @@ LAMB_API int lamb_get_trust(lamb_handle* h, float* host_out, int32_t n_tensors);
  * CUDA event monitor (after the per-rank CUDA-event timing of MegaScale's
  * guided-reading digest, section 7: critical segments are timed with CUDA
  * events instead of host timers, so timing forces no synchronisation and can
- * stay on).  With timing enabled, lamb_step records an event before its first
- * kernel and after each of its three kernels, on the handle's stream.
+ * stay on).  With timing enabled, every step records an event before its
+ * first kernel and after each of its three kernels, on the handle's stream;
+ * each of the last 64 steps keeps its own events.
  *
  *   lamb_set_timing    enable != 0 turns the monitor on (creating the events),
  *                      0 turns it off
- *   lamb_kernel_times  ms[0..3) receive the device durations, in
- *                      milliseconds, of the last step's grad-norm, moments
- *                      and apply kernels (LAMB_ERR_INVALID if the monitor is
- *                      off or no step has run since it was turned on)
+ *   lamb_step_kernel_times  ms[0..3) receive the device durations, in
+ *                      milliseconds, of step seq's grad-norm, moments and
+ *                      apply kernels, waiting for them if needed
+ *                      (LAMB_ERR_INVALID if that step was not timed or is
+ *                      older than the last 64)
+ *   lamb_kernel_times  the same for the last step enqueued
  */
 LAMB_API int lamb_set_timing(lamb_handle* h, int32_t enable);
+LAMB_API int lamb_step_kernel_times(lamb_handle* h, int64_t seq, float* ms);
 LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms);
 
 /*
@@ -257,8 +398,9 @@ LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms);
  * chunk_elems elements whose starts are multiples of 8 elements; tensors of
  * 1 .. small_max elements are packed whole, in order, into packs of at most
  * max(chunk_elems, small_max) elements and pack_max tensors; empty tensors
- * get no work.  Pack items come first, then each large tensor's chunks,
- * contiguous and in tensor order.  lamb_create picks chunk_elems itself:
+ * get no work.  Pack items come first, then the tensors of a single chunk,
+ * then the chunks of the others, each tensor's chunks contiguous and each
+ * group in tensor order.  lamb_create picks chunk_elems itself:
  * the fewest whole waves of one item per resident CTA of the GPU that keep
  * chunks at most 32768 elements, and the chunk size that fills them (never
  * below 2048).

@@ -17,6 +17,7 @@ LAMB_ERR_INVALID = -1
 LAMB_ERR_ALIGN = -2
 LAMB_ERR_CUDA = -3
 LAMB_ERR_NOMEM = -4
+LAMB_NOT_READY = 1
 LAMB_GRAD_BF16 = 0
 LAMB_GRAD_FP16 = 1
 
@@ -24,7 +25,10 @@ LAMB_GRAD_FP16 = 1
 EXPORTS = ("lamb_create", "lamb_step", "lamb_destroy", "lamb_last_error", "lamb_get_trust",
            "lamb_set_timing", "lamb_kernel_times", "lamb_plan", "lamb_plan_limits",
            "lamb_set_loss_scaler", "lamb_snapshot_async", "lamb_snapshot_wait",
-           "lamb_grad_norm_noalloc")
+           "lamb_grad_norm_noalloc", "lamb_step_async", "lamb_step_result", "lamb_set_step",
+           "lamb_loss_scale_device", "lamb_step_kernel_times", "lamb_create_sharded",
+           "lamb_split_norms", "lamb_split_moments", "lamb_split_apply",
+           "lamb_one_pass_params")
 
 
 class LambHParams(ctypes.Structure):
@@ -35,7 +39,7 @@ class LambHParams(ctypes.Structure):
 class LambResult(ctypes.Structure):
     _fields_ = [("skipped", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("grad_norm", ctypes.c_double), ("loss_scale", ctypes.c_float),
-                ("next_loss_scale", ctypes.c_float)]
+                ("next_loss_scale", ctypes.c_float), ("t", ctypes.c_int64)]
 
 
 class LambLossScaler(ctypes.Structure):
@@ -78,8 +82,27 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.lamb_create.restype = ctypes.c_int
         lib.lamb_create.argtypes = [ctypes.POINTER(P), i32, P, P, P, P, P, P,
                                     ctypes.POINTER(LambHParams), P]
+        lib.lamb_create_sharded.restype = ctypes.c_int
+        lib.lamb_create_sharded.argtypes = [ctypes.POINTER(P), i32, P, P, P, P, P, P, P, i32, P,
+                                            P, ctypes.POINTER(LambHParams), P]
+        lib.lamb_split_norms.restype = ctypes.c_int
+        lib.lamb_split_norms.argtypes = [P, P, f32]
+        lib.lamb_split_moments.restype = ctypes.c_int
+        lib.lamb_split_moments.argtypes = [P, f32, i64, f32]
+        lib.lamb_split_apply.restype = ctypes.c_int
+        lib.lamb_split_apply.argtypes = [P, ctypes.POINTER(i64)]
+        lib.lamb_one_pass_params.restype = ctypes.c_int
+        lib.lamb_one_pass_params.argtypes = [P, ctypes.POINTER(i64)]
         lib.lamb_step.restype = ctypes.c_int
         lib.lamb_step.argtypes = [P, P, f32, i64, f32, f32, ctypes.POINTER(LambResult)]
+        lib.lamb_step_async.restype = ctypes.c_int
+        lib.lamb_step_async.argtypes = [P, P, f32, f32, f32, ctypes.POINTER(i64)]
+        lib.lamb_step_result.restype = ctypes.c_int
+        lib.lamb_step_result.argtypes = [P, i64, i32, ctypes.POINTER(LambResult)]
+        lib.lamb_set_step.restype = ctypes.c_int
+        lib.lamb_set_step.argtypes = [P, i64]
+        lib.lamb_loss_scale_device.restype = ctypes.c_int
+        lib.lamb_loss_scale_device.argtypes = [P, ctypes.POINTER(P)]
         lib.lamb_destroy.restype = ctypes.c_int
         lib.lamb_destroy.argtypes = [P]
         lib.lamb_last_error.restype = ctypes.c_char_p
@@ -94,6 +117,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.lamb_snapshot_wait.argtypes = [P]
         lib.lamb_set_timing.restype = ctypes.c_int
         lib.lamb_set_timing.argtypes = [P, i32]
+        lib.lamb_step_kernel_times.restype = ctypes.c_int
+        lib.lamb_step_kernel_times.argtypes = [P, i64, P]
         lib.lamb_kernel_times.restype = ctypes.c_int
         lib.lamb_kernel_times.argtypes = [P, P]
         lib.lamb_plan.restype = ctypes.c_int

@@ -39,17 +39,23 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if any source is newer than it; return its path."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, defines=(), lib: str = LIB) -> str:
+    """Compile the library if any source is newer than it; return its path.
+
+    ``defines`` (e.g. ``["LAMB_TEST_APPLY_REPORTS_WAIT_ERROR=1"]``) and ``lib``
+    build a variant elsewhere, for tests that need a build-time hook; the
+    default builds the library itself."""
+    if not force and lib == LIB and not defines and not _stale():
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if lib == LIB else lib + ".build"
+    os.makedirs(build_dir, exist_ok=True)
     common = ["-std=c++17", "-O3", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-Wall"]
+    common += ["-D" + d for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         cmd = [nvcc, "-c", os.path.join(CSRC, src), "-o", obj] + common
         if src.endswith(".cu"):
             cmd += ARCH + ["-lineinfo", "-Xptxas", "-v" if verbose else "-O3"]
@@ -64,13 +70,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-cudart", "static"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

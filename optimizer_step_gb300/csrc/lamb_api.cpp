@@ -7,6 +7,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <new>
 #include <string>
 #include <vector>
@@ -53,6 +54,9 @@ struct DeviceGuard {
 
 void lambgb::set_last_error(const std::string& msg) { g_last_error = msg; }
 
+// Steps whose outcome stays readable after they are enqueued (lamb_step_result).
+static constexpr int kResultRing = 64;
+
 struct lamb_handle {
   int device = 0;
   cudaStream_t stream = nullptr;
@@ -61,8 +65,14 @@ struct lamb_handle {
   Plan plan;
   std::vector<int64_t> sizes;
   void* dev_block = nullptr;       // every device table and scratch array
-  void* pinned = nullptr;          // step scalars readback
-  StepScalars* scalars_host = nullptr;
+  ResultRecord* ring = nullptr;    // pinned, device-mapped: one outcome per step
+  ResultRecord* ring_dev = nullptr;  // the device's view of ring
+  cudaEvent_t ring_ev[kResultRing] = {};  // recorded after each step's last kernel
+  int64_t next_seq = 0;            // sequence number of the next step
+  int32_t split_a = 1;             // grad-norm sub-items per chunk item
+  int split_phase = 0;             // split step: 0 none, 1 norms enqueued, 2 moments enqueued
+  float split_scale = 1.0f;        // split step: the fixed loss scale of phase 1
+  float split_lr = 0.0f;           // split step: the learning rate of phase 2
   const void** grad_slot[kGradSlots] = {};        // device pointer arrays
   std::vector<const void*> slot_ptrs[kGradSlots];  // what each slot holds (empty: unused)
   int next_slot = 0;
@@ -74,24 +84,186 @@ struct lamb_handle {
   cudaEvent_t snap_done = nullptr;       // snapshot stream: copies finished
   bool snap_pending = false;             // the next step must wait for snap_done
   bool timing = false;        // CUDA event monitor on
-  bool timed_step = false;    // a step has been timed since it was turned on
-  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  int64_t timed_from = -1;    // first step timed since the monitor was turned on
+  cudaEvent_t ev[kResultRing][4] = {};  // per result slot: before / after each kernel
 };
 
 namespace {
 
 void destroy_events(lamb_handle* h) {
-  for (auto& e : h->ev) {
+  for (auto& slot : h->ev)
+    for (auto& e : slot) {
+      if (e) cudaEventDestroy(e);
+      e = nullptr;
+    }
+  h->timing = false;
+  h->timed_from = -1;
+}
+
+// Records monitor event k of result slot r on the handle's stream (no-op when
+// timing is off).
+cudaError_t mark(lamb_handle* h, int r, int k) {
+  return h->timing ? cudaEventRecord(h->ev[r][k], h->stream) : cudaSuccess;
+}
+
+// Frees what lamb_create allocated (everything may be NULL).
+void release(lamb_handle* h) {
+  for (auto& e : h->ring_ev) {
     if (e) cudaEventDestroy(e);
     e = nullptr;
   }
-  h->timing = false;
-  h->timed_step = false;
+  if (h->ring) cudaFreeHost(h->ring);
+  if (h->dev_block) cudaFree(h->dev_block);
+  h->ring = nullptr;
+  h->dev_block = nullptr;
 }
 
-// Records monitor event k on the handle's stream (no-op when timing is off).
-cudaError_t mark(lamb_handle* h, int k) {
-  return h->timing ? cudaEventRecord(h->ev[k], h->stream) : cudaSuccess;
+bool check_step_args(lamb_handle* h, const void* const* grads, float lr, float clip,
+                     float loss_scale, int* rc) {
+  if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale)) {
+    *rc = fail(LAMB_ERR_INVALID, "loss_scale must be finite and > 0");
+    return false;
+  }
+  if (!std::isfinite(lr)) {
+    *rc = fail(LAMB_ERR_INVALID, "lr must be finite");
+    return false;
+  }
+  if (std::isnan(clip)) {
+    *rc = fail(LAMB_ERR_INVALID, "clip is NaN");
+    return false;
+  }
+  if (h->n_tensors > 0 && !grads) {
+    *rc = fail(LAMB_ERR_INVALID, "grads is NULL");
+    return false;
+  }
+  for (int32_t i = 0; i < h->n_tensors; ++i) {
+    if (h->sizes[size_t(i)] == 0) continue;
+    if (!grads[i]) {
+      *rc = fail(LAMB_ERR_INVALID, "grads[" + std::to_string(i) + "] is NULL");
+      return false;
+    }
+    if (!aligned16(grads[i])) {
+      *rc = fail(LAMB_ERR_ALIGN, "grads[" + std::to_string(i) + "] is not 16-byte aligned");
+      return false;
+    }
+  }
+  return true;
+}
+
+// Enqueues one step (arguments already checked) on the handle's stream: the
+// grad pointers if new, the three kernels, and the event of its result slot.
+// t_host >= 1 fixes the step number; 0 takes it from the device counter.
+int select_grads(lamb_handle* h, const void* const* grads) {
+  // Find this step's grad pointers among the device slots, or write them
+  // into the next slot.  The write is a kernel on the handle's stream, so it
+  // runs after every earlier step has finished reading that slot.
+  const size_t nt = size_t(h->n_tensors);
+  int slot = -1;
+  for (int k = 0; k < kGradSlots && slot < 0; ++k) {
+    if (h->slot_ptrs[k].size() == nt &&
+        std::memcmp(h->slot_ptrs[k].data(), grads, nt * sizeof(void*)) == 0)
+      slot = k;
+  }
+  if (slot < 0) {
+    slot = h->next_slot;
+    h->next_slot = (h->next_slot + 1) % kGradSlots;
+    h->slot_ptrs[slot].clear();
+    const int rc = write_grad_ptrs(h->grad_slot[slot], grads, h->n_tensors, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "writing grad pointers");
+    h->slot_ptrs[slot].assign(grads, grads + nt);
+  }
+  h->T.grads = h->grad_slot[slot];
+  return LAMB_OK;
+}
+
+Hyper make_hyper(const lamb_handle* h, float lr, int64_t seq) {
+  Hyper hy;
+  hy.b1 = h->hp.beta1;
+  hy.b2 = h->hp.beta2;
+  hy.omb1 = float(1.0 - double(h->hp.beta1));
+  hy.omb2 = float(1.0 - double(h->hp.beta2));
+  hy.eps = h->hp.eps;
+  hy.lr = lr;
+  hy.slot = h->ring_dev + seq % kResultRing;
+  hy.parity = int32_t(seq & 1);
+  return hy;
+}
+
+NormArgs make_norm_args(const lamb_handle* h, float clip, int64_t t_host, int64_t seq,
+                        int32_t partial) {
+  NormArgs na;
+  na.clip = clip;
+  na.b1 = h->hp.beta1;
+  na.b2 = h->hp.beta2;
+  na.t_host = t_host;
+  na.p1_host = t_host > 0 ? std::pow(double(h->hp.beta1), double(t_host)) : 0.0;
+  na.p2_host = t_host > 0 ? std::pow(double(h->hp.beta2), double(t_host)) : 0.0;
+  na.slot = partial ? nullptr : h->ring_dev + seq % kResultRing;
+  na.split = h->split_a;
+  na.parity = int32_t(seq & 1);
+  na.partial = partial;
+  return na;
+}
+
+int wait_for_snapshot(lamb_handle* h) {
+  if (h->snap_pending) {
+    // A snapshot of the state taken before this step may still be copying:
+    // the kernels that write the state wait for it (on the GPU only).
+    const cudaError_t ce = cudaStreamWaitEvent(h->stream, h->snap_done, 0);
+    if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the snapshot copies");
+    h->snap_pending = false;
+  }
+  return LAMB_OK;
+}
+
+// Enqueues one step (arguments already checked) on the handle's stream: the
+// grad pointers if new, the three kernels, and the event of its result slot.
+// t_host >= 1 fixes the step number; 0 takes it from the device counter.
+int enqueue_step(lamb_handle* h, const void* const* grads, float lr, int64_t t_host, float clip,
+                 float loss_scale, int64_t* seq_out) {
+  cudaError_t ce;
+  int rc = select_grads(h, grads);
+  if (rc) return rc;
+  const int64_t seq = h->next_seq;
+  const int r = int(seq % kResultRing);
+  const Hyper hy = make_hyper(h, lr, seq);
+  const NormArgs na = make_norm_args(h, clip, t_host, seq, 0);
+  if ((ce = mark(h, r, 0)) != cudaSuccess) return cuda_fail(ce, "event record");
+  ScaleArgs sa = h->scaler;
+  sa.fixed = loss_scale;
+  rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, na, sa, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
+  if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
+  if ((ce = mark(h, r, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
+  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
+  if ((ce = mark(h, r, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
+  rc = launch_apply(h->T, h->grid[2], hy, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+  if ((ce = mark(h, r, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
+  if ((ce = cudaEventRecord(h->ring_ev[r], h->stream)) != cudaSuccess)
+    return cuda_fail(ce, "event record");
+  h->next_seq = seq + 1;
+  if (h->timing && h->timed_from < 0) h->timed_from = seq;
+  *seq_out = seq;
+  return LAMB_OK;
+}
+
+// Copies a finished step's outcome out of its ring slot.
+int read_result(lamb_handle* h, int64_t seq, lamb_result* out) {
+  const ResultRecord* rec = h->ring + seq % kResultRing;
+  std::atomic_thread_fence(std::memory_order_acquire);
+  const volatile ResultRecord* v = rec;
+  out->skipped = v->skipped;
+  out->reserved = 0;
+  out->grad_norm = v->grad_norm;
+  out->loss_scale = v->scale_used;
+  out->next_loss_scale = v->scale_next;
+  out->t = v->t_used;
+  if (v->error)
+    return fail(LAMB_ERR_CUDA, "a bounded wait on the GPU gave up (staged copies did not "
+                               "arrive); the state of this step is undefined");
+  return LAMB_OK;
 }
 
 }  // namespace
@@ -100,10 +272,12 @@ extern "C" {
 
 LAMB_API const char* lamb_last_error(void) { return g_last_error.c_str(); }
 
-LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
-                         const uint8_t* wd_flags, float* const* w, float* const* m,
-                         float* const* v, uint16_t* const* w_bf16, const lamb_hparams* hp,
-                         void* stream) {
+LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
+                                 const uint8_t* wd_flags, float* const* w, float* const* m,
+                                 float* const* v, uint16_t* const* w_bf16,
+                                 const int32_t* exchange_slot, int32_t n_slots,
+                                 double* norm_exchange, double* tensor_exchange,
+                                 const lamb_hparams* hp, void* stream) {
   g_last_error.clear();
   if (!out) return fail(LAMB_ERR_INVALID, "out is NULL");
   *out = nullptr;
@@ -119,6 +293,28 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
     return fail(LAMB_ERR_INVALID, "grad_dtype must be LAMB_GRAD_BF16 or LAMB_GRAD_FP16");
   if (n_tensors > 0 && (!sizes || !wd_flags || !w || !m || !v || !w_bf16))
     return fail(LAMB_ERR_INVALID, "sizes, wd_flags and the pointer arrays must be non-NULL");
+  if (n_slots < 0) return fail(LAMB_ERR_INVALID, "n_slots must be >= 0");
+  if (n_slots > 0 && !exchange_slot)
+    return fail(LAMB_ERR_INVALID, "exchange_slot is NULL but n_slots > 0");
+  if (n_slots > 0 && !tensor_exchange)
+    return fail(LAMB_ERR_INVALID, "tensor_exchange is NULL but n_slots > 0");
+  if ((reinterpret_cast<uintptr_t>(norm_exchange) & 7u) ||
+      (reinterpret_cast<uintptr_t>(tensor_exchange) & 7u))
+    return fail(LAMB_ERR_ALIGN, "the exchange buffers must be 8-byte aligned");
+  std::vector<uint8_t> no_pack(size_t(std::max(n_tensors, 0)), 0);
+  if (exchange_slot) {
+    std::vector<uint8_t> used(size_t(n_slots), 0);
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const int32_t k = exchange_slot[i];
+      if (k < -1 || k >= n_slots)
+        return fail(LAMB_ERR_INVALID, "exchange_slot[" + std::to_string(i) + "] must be -1 or in [0, n_slots)");
+      if (k < 0) continue;
+      if (used[size_t(k)])
+        return fail(LAMB_ERR_INVALID, "exchange slot " + std::to_string(k) + " is given to two tensors");
+      used[size_t(k)] = 1;
+      no_pack[size_t(i)] = 1;
+    }
+  }
   for (int32_t i = 0; i < n_tensors; ++i) {
     if (sizes[i] < 0) return fail(LAMB_ERR_INVALID, "sizes[" + std::to_string(i) + "] < 0");
     if (sizes[i] == 0) continue;
@@ -148,7 +344,7 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   if (!h) return fail(LAMB_ERR_NOMEM, "host allocation failed");
   std::string err;
   const int64_t chunk = choose_chunk(n_params, int64_t(sms) * per_sm[1]);
-  if (!build_plan(n_tensors, sizes, chunk, &h->plan, &err)) {
+  if (!build_plan(n_tensors, sizes, chunk, no_pack.data(), &h->plan, &err)) {
     delete h;
     return fail(LAMB_ERR_INVALID, err);
   }
@@ -170,7 +366,7 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
     td[i].wd = wd_flags[i] ? hp->weight_decay : 0.0f;
     td[i].first_item = h->plan.first_item[i];
     td[i].n_items = h->plan.n_items[i];
-    td[i].pad = 0;
+    td[i].xslot = exchange_slot ? exchange_slot[i] : -1;
   }
   std::vector<float> ones(nt, 1.0f);
   h->td_host = td;
@@ -192,20 +388,29 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   const size_t o_ticket = carve(nt * sizeof(uint32_t));
   const size_t o_trust = carve(nt * sizeof(float));
   const size_t o_sc = carve(sizeof(StepScalars));
-  const size_t o_queue = carve(2 * sizeof(uint32_t));
+  const size_t o_queue = carve(4 * sizeof(uint32_t));
   ce = cudaMalloc(&h->dev_block, off);
   if (ce != cudaSuccess) {
     delete h;
     return cuda_fail(ce, "cudaMalloc of the work table");
   }
-  ce = cudaMallocHost(&h->pinned, sizeof(StepScalars));
+  void* ring = nullptr;
+  ce = cudaHostAlloc(&ring, kResultRing * sizeof(ResultRecord), cudaHostAllocMapped);
+  if (ce == cudaSuccess) {
+    h->ring = static_cast<ResultRecord*>(ring);
+    std::memset(ring, 0, kResultRing * sizeof(ResultRecord));
+    void* dv = nullptr;
+    ce = cudaHostGetDevicePointer(&dv, ring, 0);
+    h->ring_dev = static_cast<ResultRecord*>(dv);
+  }
+  for (int k = 0; k < kResultRing && ce == cudaSuccess; ++k)
+    ce = cudaEventCreateWithFlags(&h->ring_ev[k], cudaEventDisableTiming);
   if (ce != cudaSuccess) {
-    cudaFree(h->dev_block);
+    release(h);
     delete h;
-    return cuda_fail(ce, "cudaMallocHost");
+    return cuda_fail(ce, "allocating the result ring");
   }
   char* base = static_cast<char*>(h->dev_block);
-  h->scalars_host = static_cast<StepScalars*>(h->pinned);
   for (int k = 0; k < kGradSlots; ++k)
     h->grad_slot[k] = reinterpret_cast<const void**>(base + o_slot[k]);
   DevTables& T = h->T;
@@ -219,124 +424,217 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
   T.trust = reinterpret_cast<float*>(base + o_trust);
   T.sc = reinterpret_cast<StepScalars*>(base + o_sc);
   T.queue = reinterpret_cast<uint32_t*>(base + o_queue);
+  T.xn = norm_exchange;
+  T.xt = tensor_exchange;
   T.n_items = int32_t(ni);
+  T.n_tensors = n_tensors;
 
   auto up = [&](size_t o, const void* src, size_t bytes) {
     return bytes ? cudaMemcpyAsync(base + o, src, bytes, cudaMemcpyHostToDevice, h->stream)
                  : cudaSuccess;
   };
+  int krc = 0;
   if ((ce = cudaMemsetAsync(h->dev_block, 0, off, h->stream)) != cudaSuccess ||
       (ce = up(o_td, td.data(), nt * sizeof(TensorDesc))) != cudaSuccess ||
       (ce = up(o_items, h->plan.items.data(), ni * sizeof(lamb_work_item))) != cudaSuccess ||
       (ce = up(o_pack, h->plan.pack_ids.data(), np * sizeof(int32_t))) != cudaSuccess ||
       (ce = up(o_trust, ones.data(), nt * sizeof(float))) != cudaSuccess ||
+      (krc = launch_set_step(T.sc, 1, double(hp->beta1), double(hp->beta2), h->stream)) != 0 ||
       (ce = cudaStreamSynchronize(h->stream)) != cudaSuccess) {
-    cudaFreeHost(h->pinned);
-    cudaFree(h->dev_block);
+    if (krc) ce = cudaError_t(krc);
+    release(h);
     delete h;
     return cuda_fail(ce, "uploading the work table");
   }
 
-  // Persistent grids: as many CTAs as fit at once, never more than the items.
+  // Persistent grids: as many CTAs as fit at once, never more than the items
+  // (the grad-norm kernel: never more than its sub-items).
+  int64_t n_chunk_items = 0;
+  for (const auto& it : h->plan.items) n_chunk_items += it.tensor >= 0;
   for (int k = 0; k < 3; ++k) {
     const int64_t full = int64_t(per_sm[k]) * sms;
     h->grid[k] = int(std::max<int64_t>(1, std::min<int64_t>(full, int64_t(ni))));
   }
+  // Sub-items per chunk item for the grad-norm kernel: about kSplitTarget per
+  // CTA of its full grid, sub-items of at least kMinSubItem elements.
+  {
+    const int64_t full = int64_t(per_sm[0]) * sms;
+    int64_t split = n_chunk_items > 0 ? (kSplitTarget * full + n_chunk_items - 1) / n_chunk_items
+                                      : 1;
+    const int64_t chunk_cap = std::max<int64_t>(1, chunk / kMinSubItem);
+    split = std::max<int64_t>(1, std::min<int64_t>(split, std::min<int64_t>(kMaxSplit, chunk_cap)));
+    h->split_a = int32_t(split);
+    h->grid[0] = int(std::max<int64_t>(
+        1, std::min<int64_t>(full, int64_t(ni - n_chunk_items) + n_chunk_items * split)));
+  }
   *out = h;
   return LAMB_OK;
+}
+
+LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
+                         const uint8_t* wd_flags, float* const* w, float* const* m,
+                         float* const* v, uint16_t* const* w_bf16, const lamb_hparams* hp,
+                         void* stream) {
+  return lamb_create_sharded(out, n_tensors, sizes, wd_flags, w, m, v, w_bf16, nullptr, 0,
+                             nullptr, nullptr, hp, stream);
 }
 
 LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
                        float loss_scale, lamb_result* out) {
   g_last_error.clear();
   if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (h->split_phase != 0) return fail(LAMB_ERR_INVALID, "a split step is in progress");
   if (!out) return fail(LAMB_ERR_INVALID, "out is NULL");
   if (t < 1) return fail(LAMB_ERR_INVALID, "t must be >= 1");
-  if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
-    return fail(LAMB_ERR_INVALID, "loss_scale must be finite and > 0");
-  if (!std::isfinite(lr)) return fail(LAMB_ERR_INVALID, "lr must be finite");
-  if (std::isnan(clip)) return fail(LAMB_ERR_INVALID, "clip is NaN");
-  if (h->n_tensors > 0 && !grads) return fail(LAMB_ERR_INVALID, "grads is NULL");
-  for (int32_t i = 0; i < h->n_tensors; ++i) {
-    if (h->sizes[size_t(i)] == 0) continue;
-    if (!grads[i]) return fail(LAMB_ERR_INVALID, "grads[" + std::to_string(i) + "] is NULL");
-    if (!aligned16(grads[i]))
-      return fail(LAMB_ERR_ALIGN, "grads[" + std::to_string(i) + "] is not 16-byte aligned");
-  }
-  out->skipped = 0;
-  out->reserved = 0;
-  out->grad_norm = 0.0;
+  int rc = LAMB_OK;
+  if (!check_step_args(h, grads, lr, clip, loss_scale, &rc)) return rc;
+  std::memset(out, 0, sizeof *out);
   out->loss_scale = loss_scale;
   out->next_loss_scale = loss_scale;
   // An empty shard still runs the (empty) kernels: the grad norm is 0 and a
   // dynamic loss scale still advances.
-
   DeviceGuard dg(h->device);
   if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
-  cudaError_t ce;
-  // Find this step's grad pointers among the device slots, or write them
-  // into the next slot.  No slot is in use: every earlier step waited for its
-  // stream before returning.
-  const size_t nt = size_t(h->n_tensors);
-  int slot = -1;
-  for (int k = 0; k < kGradSlots && slot < 0; ++k) {
-    if (h->slot_ptrs[k].size() == nt &&
-        std::memcmp(h->slot_ptrs[k].data(), grads, nt * sizeof(void*)) == 0)
-      slot = k;
-  }
-  if (slot < 0) {
-    slot = h->next_slot;
-    h->next_slot = (h->next_slot + 1) % kGradSlots;
-    h->slot_ptrs[slot].clear();
-    const int rc = write_grad_ptrs(h->grad_slot[slot], grads, h->n_tensors, h->stream);
-    if (rc) return cuda_fail(cudaError_t(rc), "writing grad pointers");
-    h->slot_ptrs[slot].assign(grads, grads + nt);
-  }
-  h->T.grads = h->grad_slot[slot];
+  int64_t seq = 0;
+  if ((rc = enqueue_step(h, grads, lr, t, clip, loss_scale, &seq)) != LAMB_OK) return rc;
+  const cudaError_t ce = cudaEventSynchronize(h->ring_ev[seq % kResultRing]);
+  if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the step");
+  return read_result(h, seq, out);
+}
 
-  const double b1 = h->hp.beta1, b2 = h->hp.beta2;
-  Hyper hy;
-  hy.b1 = h->hp.beta1;
-  hy.b2 = h->hp.beta2;
-  hy.omb1 = float(1.0 - b1);
-  hy.omb2 = float(1.0 - b2);
-  hy.c1 = float(1.0 / (1.0 - std::pow(b1, double(t))));
-  hy.c2 = float(1.0 / (1.0 - std::pow(b2, double(t))));
-  hy.eps = h->hp.eps;
-  hy.lr = lr;
+LAMB_API int lamb_step_async(lamb_handle* h, const void* const* grads, float lr, float clip,
+                             float loss_scale, int64_t* seq) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (h->split_phase != 0) return fail(LAMB_ERR_INVALID, "a split step is in progress");
+  int rc = LAMB_OK;
+  if (!check_step_args(h, grads, lr, clip, loss_scale, &rc)) return rc;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  int64_t s = 0;
+  if ((rc = enqueue_step(h, grads, lr, 0, clip, loss_scale, &s)) != LAMB_OK) return rc;
+  if (seq) *seq = s;
+  return LAMB_OK;
+}
 
-  if ((ce = mark(h, 0)) != cudaSuccess) return cuda_fail(ce, "event record");
+LAMB_API int lamb_step_result(lamb_handle* h, int64_t seq, int32_t wait, lamb_result* out) {
+  g_last_error.clear();
+  if (!h || !out) return fail(LAMB_ERR_INVALID, "NULL argument");
+  if (seq < 0 || seq >= h->next_seq)
+    return fail(LAMB_ERR_INVALID, "no step with sequence number " + std::to_string(seq));
+  if (seq < h->next_seq - kResultRing)
+    return fail(LAMB_ERR_INVALID, "the outcome of step " + std::to_string(seq) +
+                                      " was overwritten: only the last " +
+                                      std::to_string(kResultRing) + " steps are kept");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  cudaEvent_t ev = h->ring_ev[seq % kResultRing];
+  const cudaError_t ce = wait ? cudaEventSynchronize(ev) : cudaEventQuery(ev);
+  if (ce == cudaErrorNotReady) return LAMB_NOT_READY;
+  if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the step");
+  return read_result(h, seq, out);
+}
+
+LAMB_API int lamb_split_norms(lamb_handle* h, const void* const* grads, float loss_scale) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (!h->T.xn)
+    return fail(LAMB_ERR_INVALID, "no norm exchange buffer: create the handle with "
+                                  "lamb_create_sharded");
+  if (h->split_phase != 0) return fail(LAMB_ERR_INVALID, "a split step is already in progress");
+  int rc = LAMB_OK;
+  if (!check_step_args(h, grads, 0.0f, 0.0f, loss_scale, &rc)) return rc;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  if ((rc = select_grads(h, grads)) != LAMB_OK) return rc;
+  const int64_t seq = h->next_seq;
+  const int r = int(seq % kResultRing);
+  cudaError_t ce = mark(h, r, 0);
+  if (ce != cudaSuccess) return cuda_fail(ce, "event record");
   ScaleArgs sa = h->scaler;
   sa.fixed = loss_scale;
-  int rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, clip, sa, h->stream);
+  rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, make_norm_args(h, 0.0f, 0, seq, 1),
+                        sa, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
-  if (h->snap_pending) {
-    // A snapshot of the state taken before this step may still be copying:
-    // the kernels that write the state wait for it (on the GPU only).
-    if ((ce = cudaStreamWaitEvent(h->stream, h->snap_done, 0)) != cudaSuccess)
-      return cuda_fail(ce, "waiting for the snapshot copies");
-    h->snap_pending = false;
-  }
-  if ((ce = mark(h, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
+  h->split_scale = loss_scale;
+  h->split_phase = 1;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_split_moments(lamb_handle* h, float lr, int64_t t, float clip) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (h->split_phase != 1) return fail(LAMB_ERR_INVALID, "call lamb_split_norms first");
+  if (t < 0) return fail(LAMB_ERR_INVALID, "t must be >= 1, or 0 for the GPU's step counter");
+  if (!std::isfinite(lr)) return fail(LAMB_ERR_INVALID, "lr must be finite");
+  if (std::isnan(clip)) return fail(LAMB_ERR_INVALID, "clip is NaN");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  const int64_t seq = h->next_seq;
+  const int r = int(seq % kResultRing);
+  ScaleArgs sa = h->scaler;
+  sa.fixed = h->split_scale;
+  int rc = launch_finalize(h->T, make_norm_args(h, clip, t, seq, 0), sa, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "finalize kernel launch");
+  if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
+  cudaError_t ce = mark(h, r, 1);
+  if (ce != cudaSuccess) return cuda_fail(ce, "event record");
+  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, make_hyper(h, lr, seq), h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
-  if ((ce = mark(h, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_apply(h->T, h->grid[2], hy, h->stream);
+  h->split_lr = lr;
+  h->split_phase = 2;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq_out) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (h->split_phase != 2) return fail(LAMB_ERR_INVALID, "call lamb_split_moments first");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  const int64_t seq = h->next_seq;
+  const int r = int(seq % kResultRing);
+  cudaError_t ce = mark(h, r, 2);
+  if (ce != cudaSuccess) return cuda_fail(ce, "event record");
+  int rc = launch_exchange_trust(h->T, h->stream);
+  if (rc) return cuda_fail(cudaError_t(rc), "trust kernel launch");
+  rc = launch_apply(h->T, h->grid[2], make_hyper(h, h->split_lr, seq), h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
-  if ((ce = mark(h, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
-  ce = cudaMemcpyAsync(h->scalars_host, h->T.sc, sizeof(StepScalars), cudaMemcpyDeviceToHost,
-                       h->stream);
-  if (ce != cudaSuccess) return cuda_fail(ce, "reading the step result");
-  ce = cudaStreamSynchronize(h->stream);
-  if (ce != cudaSuccess) return cuda_fail(ce, "waiting for the step");
-  if (h->scalars_host->error)
-    return fail(LAMB_ERR_CUDA, "a bounded wait on the GPU gave up (staged copies did not "
-                               "arrive); the state of this step is undefined");
-  out->skipped = h->scalars_host->skip;
-  out->grad_norm = h->scalars_host->grad_norm;
-  out->loss_scale = h->scalars_host->scale_used;
-  out->next_loss_scale = h->scaler.dynamic ? h->scalars_host->scale : loss_scale;
-  if (h->timing) h->timed_step = true;
+  if ((ce = mark(h, r, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
+  if ((ce = cudaEventRecord(h->ring_ev[r], h->stream)) != cudaSuccess)
+    return cuda_fail(ce, "event record");
+  h->next_seq = seq + 1;
+  if (h->timing && h->timed_from < 0) h->timed_from = seq;
+  h->split_phase = 0;
+  if (seq_out) *seq_out = seq;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_one_pass_params(lamb_handle* h, int64_t* n) {
+  g_last_error.clear();
+  if (!h || !n) return fail(LAMB_ERR_INVALID, "NULL argument");
+  int64_t total = 0;
+  for (const TensorDesc& d : h->td_host)
+    if (d.n > 0 && d.xslot < 0 && (d.n_items == 0 || d.n_items == 1)) total += d.n;
+  *n = total;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_set_step(lamb_handle* h, int64_t t) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (t < 1) return fail(LAMB_ERR_INVALID, "t must be >= 1");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  const int rc = launch_set_step(h->T.sc, t, std::pow(double(h->hp.beta1), double(t)),
+                                 std::pow(double(h->hp.beta2), double(t)), h->stream);
+  return rc ? cuda_fail(cudaError_t(rc), "setting the step number") : LAMB_OK;
+}
+
+LAMB_API int lamb_loss_scale_device(lamb_handle* h, const float** scale) {
+  g_last_error.clear();
+  if (!h || !scale) return fail(LAMB_ERR_INVALID, "NULL argument");
+  *scale = &h->T.sc->scale;
   return LAMB_OK;
 }
 
@@ -388,31 +686,44 @@ LAMB_API int lamb_set_timing(lamb_handle* h, int32_t enable) {
     return ce == cudaSuccess ? LAMB_OK : cuda_fail(ce, "waiting for the stream");
   }
   if (h->timing) return LAMB_OK;
-  for (auto& e : h->ev) {
-    cudaError_t ce = cudaEventCreate(&e);
-    if (ce != cudaSuccess) {
-      destroy_events(h);
-      return cuda_fail(ce, "cudaEventCreate");
+  for (auto& slot : h->ev)
+    for (auto& e : slot) {
+      cudaError_t ce = cudaEventCreate(&e);
+      if (ce != cudaSuccess) {
+        destroy_events(h);
+        return cuda_fail(ce, "cudaEventCreate");
+      }
     }
-  }
   h->timing = true;
-  h->timed_step = false;
+  h->timed_from = -1;
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_step_kernel_times(lamb_handle* h, int64_t seq, float* ms) {
+  g_last_error.clear();
+  if (!h || !ms) return fail(LAMB_ERR_INVALID, "NULL argument");
+  if (!h->timing || h->timed_from < 0 || seq < h->timed_from || seq >= h->next_seq ||
+      seq < h->next_seq - kResultRing)
+    return fail(LAMB_ERR_INVALID, "step " + std::to_string(seq) +
+                                      " was not timed: enable the monitor first; only the "
+                                      "last 64 steps are kept");
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  cudaEvent_t* ev = h->ev[seq % kResultRing];
+  for (int k = 0; k < 3; ++k) {
+    cudaError_t ce = cudaEventSynchronize(ev[k + 1]);
+    if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms[k], ev[k], ev[k + 1]);
+    if (ce != cudaSuccess) return cuda_fail(ce, "reading monitor events");
+  }
   return LAMB_OK;
 }
 
 LAMB_API int lamb_kernel_times(lamb_handle* h, float* ms) {
   g_last_error.clear();
   if (!h || !ms) return fail(LAMB_ERR_INVALID, "NULL argument");
-  if (!h->timing || !h->timed_step)
+  if (!h->timing || h->timed_from < 0)
     return fail(LAMB_ERR_INVALID, "no timed step: enable the monitor and run a step first");
-  DeviceGuard dg(h->device);
-  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
-  for (int k = 0; k < 3; ++k) {
-    cudaError_t ce = cudaEventSynchronize(h->ev[k + 1]);
-    if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms[k], h->ev[k], h->ev[k + 1]);
-    if (ce != cudaSuccess) return cuda_fail(ce, "reading monitor events");
-  }
-  return LAMB_OK;
+  return lamb_step_kernel_times(h, h->next_seq - 1, ms);
 }
 
 LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* const* host_m,
@@ -494,8 +805,7 @@ LAMB_API int lamb_destroy(lamb_handle* h) {
       cudaEventDestroy(h->snap_done);
     }
     if (h->snap_start) cudaEventDestroy(h->snap_start);
-    if (h->pinned) cudaFreeHost(h->pinned);
-    if (h->dev_block) cudaFree(h->dev_block);
+    release(h);
   }
   delete h;
   return rc;

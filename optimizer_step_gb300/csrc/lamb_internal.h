@@ -23,6 +23,15 @@ constexpr int64_t kChunkElems = 32768;
 constexpr int64_t kMinChunkElems = 2048;
 constexpr int64_t kSmallMax = 4096;
 constexpr int64_t kPackMax = 64;
+// The grad-norm kernel cuts each chunk item into sub-items: about
+// kSplitTarget per CTA of its grid, at most kMaxSplit per item, each at least
+// kMinSubItem elements.
+#ifndef LAMB_SPLIT_TARGET
+#define LAMB_SPLIT_TARGET 6
+#endif
+constexpr int64_t kSplitTarget = LAMB_SPLIT_TARGET;
+constexpr int64_t kMaxSplit = 16;
+constexpr int64_t kMinSubItem = 1024;
 
 // Chunk size for n_params elements on a GPU with cta_slots resident CTAs.
 int64_t choose_chunk(int64_t n_params, int64_t cta_slots);
@@ -35,9 +44,10 @@ struct Plan {
 };
 
 // Builds the work table; returns false (with a message) on invalid sizes or
-// a table too large for 32-bit item indices.
-bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems, Plan* plan,
-                std::string* err);
+// a table too large for 32-bit item indices.  Tensors with no_pack[i] != 0
+// (no_pack may be NULL) get chunk items even when small.
+bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
+                const uint8_t* no_pack, Plan* plan, std::string* err);
 
 // Per-tensor record the kernels read (device copy built at create time).
 struct TensorDesc {
@@ -49,11 +59,11 @@ struct TensorDesc {
   float wd;            // weight_decay if the tensor's flag is set, else 0
   int32_t first_item;  // first chunk item of a chunked tensor
   int32_t n_items;     // number of chunk items (0 for packed tensors)
-  int32_t pad;
+  int32_t xslot;       // -1, or the exchange slot of a tensor shared with other ranks
 };
 
 // Device-resident values of one step, written by the grad-norm kernel's last
-// CTA and read by the two later kernels and by the host.
+// CTA and read by the two later kernels.
 struct StepScalars {
   double grad_norm;    // ||g / S|| (+inf if skipped)
   float gscale;        // c / S, the factor turning a raw grad into g'
@@ -64,6 +74,36 @@ struct StepScalars {
   float scale;         // dynamic loss scale for the next step
   int32_t good_steps;  // clean steps in a row since the last growth/backoff
   int32_t error;       // set on the GPU if a bounded wait gave up this step
+  float c1, c2;        // 1/(1-beta1^t), 1/(1-beta2^t) of this step
+  int64_t t_used;      // the step number t of this step
+  int64_t t_next;      // the step number of the next step (advances on clean steps)
+  double p1_next;      // beta1^t_next and beta2^t_next (fp64; the host's pow when t
+  double p2_next;      //   is set, then one multiplication per step that is not skipped)
+};
+
+// The outcome of one step as the host reads it: written by the GPU straight
+// into a slot of the handle's pinned, device-mapped result ring (the grad-norm
+// kernel's last CTA writes all of it; a CTA of the apply kernel whose bounded
+// wait gives up sets error).
+struct ResultRecord {
+  double grad_norm;
+  int64_t t_used;
+  float scale_used;
+  float scale_next;
+  int32_t skipped;
+  int32_t error;
+};
+
+// Step-level arguments of the grad-norm kernel.
+struct NormArgs {
+  float clip;           // <= 0: no clipping
+  float b1, b2;         // beta1, beta2 (the bias corrections are formed on the GPU)
+  int64_t t_host;       // >= 1: this step's t; 0: take it from StepScalars::t_next
+  double p1_host, p2_host;  // beta1^t_host and beta2^t_host (host pow) when t_host >= 1
+  ResultRecord* slot;   // device view of this step's result slot
+  int32_t split;        // sub-items per chunk item (balances the CTAs)
+  int32_t parity;       // this step's sequence number & 1
+  int32_t partial;      // 1: only write this shard's {sum g^2, inf/NaN} to DevTables::xn
 };
 
 // How the grad-norm kernel finds this step's loss scale.
@@ -85,14 +125,18 @@ struct DevTables {
   uint32_t* tensor_ticket;   // per tensor: chunk items finished this step
   float* trust;              // per tensor: trust ratio of this step
   StepScalars* sc;
-  uint32_t* queue;           // [2] item counters of the moments and apply kernels
+  uint32_t* queue;           // [4] item counters: moments [parity], apply [2 + parity]
+  double* xn;                // split step: {sum of raw g^2, inf/NaN flag} (caller-owned)
+  double* xt;                // split step: {sum w^2, sum r^2} per exchange slot (caller-owned)
   int32_t n_items;
+  int32_t n_tensors;
 };
 
 struct Hyper {
   float b1, b2, omb1, omb2;  // beta1, beta2, 1-beta1, 1-beta2
-  float c1, c2;              // 1/(1-beta1^t), 1/(1-beta2^t)
   float eps, lr;
+  ResultRecord* slot;        // device view of this step's result slot
+  int32_t parity;            // this step's sequence number & 1: which item counters it uses
 };
 
 // Sets the calling thread's message returned by lamb_last_error().
@@ -102,8 +146,16 @@ void set_last_error(const std::string& msg);
 // max_blocks_per_sm: CTAs per SM a kernel's persistent grid uses (what fits,
 // capped per kernel); kernel 0 norm, 1 moments, 2 apply; negative: CUDA error.
 int max_blocks_per_sm(int kernel, int grad_dtype);
-int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip,
+int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, const NormArgs& na,
                      const ScaleArgs& sa, void* stream);
+// Sets StepScalars::t_next (the step number of the next step) and its
+// powers beta1^t, beta2^t on the stream.
+int launch_set_step(StepScalars* sc, int64_t t, double p1, double p2, void* stream);
+// Split step: forms the step's scalars from the group's summed DevTables::xn
+// (what the grad-norm kernel's last CTA does in an ordinary step).
+int launch_finalize(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, void* stream);
+// Split step: trust ratios of exchanged tensors from the group's summed xt.
+int launch_exchange_trust(const DevTables& T, void* stream);
 int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream);
 int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream);
 

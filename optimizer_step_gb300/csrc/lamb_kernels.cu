@@ -20,8 +20,9 @@
 //      bulk copies) and writes w and the bf16 copy (18 B/elem); r is
 //      recomputed with the same function as in B, so the r applied is
 //      bit-identical to the r whose norm was taken.
-// Small tensors (packs) are finished inside B by the warp that owns them, so
-// they cost 30 B/elem instead of 42: the second pass over them hits cache.
+// Small tensors (packs) are finished inside B by the warp that owns them, and
+// tensors of a single work item (at most one chunk) by the CTA that owns it,
+// so they cost 30 B/elem instead of 42: the second pass over them hits cache.
 // Recomputing r costs the same bytes as storing it (B +4 B write, C reads r
 // instead of m and v), and avoids a 4 B/param scratch buffer.
 //
@@ -87,8 +88,35 @@ namespace {
 #ifndef LAMB_REVERSE_C
 #define LAMB_REVERSE_C 1
 #endif
+// 1: the moments and apply kernels are launched as programmatic dependents
+// of the kernel before them (PDL): their CTAs start while that kernel drains,
+// take their first work item and prefetch its first bytes into L2, and only
+// then wait (griddepcontrol.wait) for it to finish before reading what it
+// wrote.  0: ordinary stream order.
+#ifndef LAMB_PDL
+#define LAMB_PDL 1
+#endif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+
+// Lets dependent grids launch (once every CTA of this grid has called it or
+// exited); they still wait for this grid to finish before using its results.
+__device__ __forceinline__ void pdl_trigger() {
+#if LAMB_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+// Waits until the grids this one depends on have finished and their memory
+// writes are visible (returns at once when launched without a dependency).
+__device__ __forceinline__ void pdl_wait() {
+#if LAMB_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+// Hint: bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // ------------------------------------------------------------ memory access
 // Everything is streamed once per kernel and the step's footprint is far
@@ -273,7 +301,7 @@ struct ItemQueue {
 // folding them into fp64 (a chunk gives each thread at most 16 vectors; a
 // packed tensor of at most 4096 elements gives each lane at most 16).
 #ifndef LAMB_LOADS_A
-#define LAMB_LOADS_A 4
+#define LAMB_LOADS_A 8
 #endif
 constexpr int kLoadsA = LAMB_LOADS_A;
 
@@ -310,30 +338,203 @@ __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int6
   total += double(acc);
 }
 
-// Each CTA walks its items (blockIdx.x, blockIdx.x + gridDim.x, ...) and
-// keeps one fp64 total per thread; one block reduction per CTA gives the
-// CTA's partial, and the CTA that finishes last (atomic ticket, nobody waits)
-// adds the gridDim.x partials in CTA order and publishes the step's scalars.
+// Publishes one step's scalars from the sum of raw g^2 over the shard (or the
+// data-parallel group) and the inf/NaN flag: the grad norm ||g/S||, the clip
+// factor, the skip flag, the step number t and its bias corrections (from
+// beta^t in fp64, rounded once to fp32; t and beta^t advance only on a step
+// that is not skipped -- fp64 is slow on GB300, so there is no pow here), the
+// dynamic loss scale, the host's copy of the outcome, and the item counters
+// of the next step.  One thread.
+__device__ void publish_step(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, double s,
+                             bool nf) {
+  StepScalars* sc = T.sc;
+  const float S = sa.dynamic ? sc->scale : sa.fixed;
+  const double loss_scale = double(S);
+  if (nf) {
+    sc->skip = 1;
+    sc->grad_norm = __longlong_as_double(0x7FF0000000000000ll);  // +inf
+    sc->gscale = 0.0f;
+  } else {
+    const double gn = sqrt(s) / loss_scale;
+    const double c = (na.clip > 0.0f && gn > double(na.clip)) ? double(na.clip) / gn : 1.0;
+    sc->skip = 0;
+    sc->grad_norm = gn;
+    sc->gscale = float(c / loss_scale);
+  }
+  sc->scale_used = S;
+  const bool host_t = na.t_host > 0;
+  const int64_t t = host_t ? na.t_host : sc->t_next;
+  const double p1 = host_t ? na.p1_host : sc->p1_next;  // beta1^t
+  const double p2 = host_t ? na.p2_host : sc->p2_next;  // beta2^t
+  sc->t_used = t;
+  sc->c1 = float(1.0 / (1.0 - p1));
+  sc->c2 = float(1.0 / (1.0 - p2));
+  sc->t_next = nf ? t : t + 1;
+  sc->p1_next = nf ? p1 : p1 * double(na.b1);
+  sc->p2_next = nf ? p2 : p2 * double(na.b2);
+  if (sa.dynamic) {
+    // Loss scale for the next step: back off after an overflow, grow after
+    // `interval` clean steps in a row (fp32 products, clamped).
+    float next = S;
+    if (nf) {
+      next = __fmul_rn(S, sa.backoff);
+      if (next < sa.min_scale) next = sa.min_scale;
+      sc->good_steps = 0;
+    } else if (++sc->good_steps == sa.interval) {
+      const float grown = __fmul_rn(S, sa.growth);
+      if (isfinite(grown)) next = grown > sa.max_scale ? sa.max_scale : grown;
+      sc->good_steps = 0;
+    }
+    sc->scale = next;
+  }
+  if (na.slot) {  // the host's copy of the outcome, in mapped pinned memory
+    volatile ResultRecord* r = na.slot;
+    r->grad_norm = sc->grad_norm;
+    r->t_used = t;
+    r->scale_used = S;
+    r->scale_next = sa.dynamic ? sc->scale : S;
+    r->skipped = nf ? 1 : 0;
+    r->error = 0;
+  }
+  sc->error = 0;  // no wait of this step has given up yet
+  // Item counters of the next step's moments and apply kernels (the other
+  // parity; this step's were reset one step ago, so this step's kernels can
+  // take items before the kernel that publishes the step has finished).
+  T.queue[1 - na.parity] = 0u;
+  T.queue[3 - na.parity] = 0u;
+}
+
+// Each chunk item is cut into na.split equal sub-items (8-element aligned)
+// so that the grid's CTAs get nearly equal shares even when the work table
+// holds only a wave or two of items; a pack item is one sub-item.  A CTA owns
+// sub-items blockIdx.x, blockIdx.x + gridDim.x, ...; it stages up to kStageA
+// of them at a time in shared memory (one thread per sub-item loads its item
+// and grad pointer, so there is one dependent-load latency per batch, not per
+// sub-item), then streams their whole 8-element vectors as one flat list:
+// each thread takes vectors tid, tid + 256, ... with kLoadsA 16-byte loads
+// in flight, across sub-item boundaries.  Each thread keeps one fp64 total
+// (fp32 partial sums of at most 8 * kLoadsA squares folded in after every
+// trip); one block reduction per CTA gives the CTA's partial, and the CTA
+// that finishes last (atomic ticket, nobody waits) adds the gridDim.x
+// partials in CTA order and publishes the step's scalars: the grad norm, the
+// clip factor, the skip flag, the step number t and its bias corrections,
+// the dynamic loss scale, and the host's copy of the outcome.
+constexpr int kStageA = 32;  // one warp stages the sub-items and scans their lengths
+static_assert(kStageA == 32, "the staging scan is one warp's shuffle scan");
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(DevTables T, float clip,
+__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(DevTables T, NormArgs na,
                                                                                ScaleArgs sa) {
   __shared__ double red[kWarps];
   __shared__ int is_last;
+  __shared__ const uint16_t* s_g[kStageA];  // first element of each staged sub-item
+  __shared__ int32_t s_len[kStageA];        // its element count (0: none)
+  __shared__ int32_t s_pack[kStageA];       // pack item index, or -1
+  __shared__ int64_t s_vend[kStageA];       // inclusive prefix of whole-vector counts
+  pdl_trigger();  // the moments kernel may launch and take its first items
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t bad = 0;
   double total = 0.0;
-  for (int32_t it = blockIdx.x; it < T.n_items; it += gridDim.x) {
-    const lamb_work_item wi = T.items[it];
-    if (wi.tensor >= 0) {
-      const uint16_t* g = static_cast<const uint16_t*>(T.grads[wi.tensor]) + wi.begin;
-      sumsq_range<DT>(g, wi.count, threadIdx.x, kThreads, total, bad);
-    } else {
+  const int32_t split = na.split;
+  const int64_t n_sub = int64_t(T.n_items) * split;
+  const int64_t stride = int64_t(kStageA) * gridDim.x;
+  for (int64_t first = blockIdx.x; first < n_sub; first += stride) {
+    if (threadIdx.x < kStageA) {
+      const int64_t vi = first + int64_t(threadIdx.x) * gridDim.x;
+      const uint16_t* g = nullptr;
+      int32_t len = 0, pack = -1;
+      if (vi < n_sub) {
+        const int32_t it = int32_t(vi / split);
+        const int32_t part = int32_t(vi - int64_t(it) * split);
+        const lamb_work_item wi = T.items[it];
+        if (wi.tensor >= 0) {
+          const int64_t per = ((int64_t(wi.count) + split - 1) / split + 7) & ~int64_t(7);
+          const int64_t b = int64_t(part) * per;
+          const int64_t e = min(int64_t(wi.count), b + per);
+          if (b < e) {
+            g = static_cast<const uint16_t*>(T.grads[wi.tensor]) + wi.begin + b;
+            len = int32_t(e - b);
+          }
+        } else if (part == 0) {
+          pack = it;
+        }
+      }
+      s_g[threadIdx.x] = g;
+      s_len[threadIdx.x] = len;
+      s_pack[threadIdx.x] = pack;
+      // Inclusive prefix of whole vectors over the staged sub-items (warp 0).
+      int64_t nv = len >> 3;
+#pragma unroll
+      for (int o = 1; o < kStageA; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, nv, o);
+        if (lane >= o) nv += y;
+      }
+      s_vend[threadIdx.x] = nv;
+    }
+    __syncthreads();
+    const int64_t nvec = s_vend[kStageA - 1];
+    // The thread's current staged sub-item, kept in registers: its vectors
+    // are [jbeg, jend) of the flat list and start at jg (a thread's vectors
+    // only increase, so it only moves forward).
+    int j = 0;
+    int64_t jbeg = 0, jend = s_vend[0];
+    const uint4* jg = reinterpret_cast<const uint4*>(s_g[0]);
+    for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += int64_t(kLoadsA) * kThreads) {
+      uint4 q[kLoadsA];
+#pragma unroll
+      for (int u = 0; u < kLoadsA; ++u) {
+        const int64_t v = v0 + int64_t(u) * kThreads;
+        if (v < nvec) {
+          while (v >= jend) {
+            ++j;
+            jbeg = jend;
+            jend = s_vend[j];
+            jg = reinterpret_cast<const uint4*>(s_g[j]);
+          }
+          q[u] = ld_policy(jg + (v - jbeg));
+        } else {
+          q[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      float acc = 0.0f;
+#pragma unroll
+      for (int u = 0; u < kLoadsA; ++u) {
+        const uint32_t wv[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f = decode2<DT>(wv[h]);
+          acc = __fmaf_rn(f.x, f.x, acc);
+          acc = __fmaf_rn(f.y, f.y, acc);
+          bad |= nonfinite2<DT>(wv[h]);
+        }
+      }
+      total += double(acc);
+    }
+    // The last (fewer than 8) elements of each staged sub-item: one thread each.
+    if (threadIdx.x < kStageA) {
+      const int32_t len = s_len[threadIdx.x];
+      const uint16_t* g = s_g[threadIdx.x];
+      float acc = 0.0f;
+      for (int32_t e = len & ~7; e < len; ++e) {
+        const uint16_t x = g[e];
+        const float f = decode1<DT>(x);
+        acc = __fmaf_rn(f, f, acc);
+        bad |= nonfinite2<DT>(uint32_t(x) | (uint32_t(x) << 16));
+      }
+      total += double(acc);
+    }
+    // Staged pack items: a warp per small tensor.
+    for (int jj = 0; jj < kStageA; ++jj) {
+      const int32_t it = s_pack[jj];
+      if (it < 0) continue;
+      const lamb_work_item wi = T.items[it];
       for (int k = warp; k < wi.count; k += kWarps) {
         const int32_t ti = T.pack_ids[wi.begin + k];
         sumsq_range<DT>(static_cast<const uint16_t*>(T.grads[ti]), T.td[ti].n, lane, 32, total,
                         bad);
       }
     }
+    __syncthreads();  // the staging arrays are refilled next
   }
   const double cta_sum = block_sum(total, red);
   bad = __syncthreads_or(bad);
@@ -351,42 +552,32 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
   for (int32_t i = threadIdx.x; i < int32_t(gridDim.x); i += kThreads) s += __ldcg(&T.item_g2[i]);
   s = block_sum(s, red);
   if (threadIdx.x == 0) {
-    StepScalars* sc = T.sc;
-    const uint32_t nf = atomicExch(&sc->nonfinite, 0u);
-    const float S = sa.dynamic ? sc->scale : sa.fixed;
-    const double loss_scale = double(S);
-    if (nf) {
-      sc->skip = 1;
-      sc->grad_norm = __longlong_as_double(0x7FF0000000000000ll);  // +inf
-      sc->gscale = 0.0f;
+    const uint32_t nf = atomicExch(&T.sc->nonfinite, 0u);
+    T.sc->ticket = 0u;  // ready for the next step
+    if (na.partial) {
+      // Split step: this shard's partials go out to be summed over the group;
+      // the finalize kernel publishes the step once they come back.
+      T.xn[0] = s;
+      T.xn[1] = nf ? 1.0 : 0.0;
     } else {
-      const double gn = sqrt(s) / loss_scale;
-      const double c = (clip > 0.0f && gn > double(clip)) ? double(clip) / gn : 1.0;
-      sc->skip = 0;
-      sc->grad_norm = gn;
-      sc->gscale = float(c / loss_scale);
+      publish_step(T, na, sa, s, nf != 0u);
     }
-    sc->scale_used = S;
-    if (sa.dynamic) {
-      // Loss scale for the next step: back off after an overflow, grow after
-      // `interval` clean steps in a row (fp32 products, clamped).
-      float next = S;
-      if (nf) {
-        next = __fmul_rn(S, sa.backoff);
-        if (next < sa.min_scale) next = sa.min_scale;
-        sc->good_steps = 0;
-      } else if (++sc->good_steps == sa.interval) {
-        const float grown = __fmul_rn(S, sa.growth);
-        if (isfinite(grown)) next = grown > sa.max_scale ? sa.max_scale : grown;
-        sc->good_steps = 0;
-      }
-      sc->scale = next;
-    }
-    sc->error = 0;    // no wait of this step has given up yet
-    sc->ticket = 0u;  // ready for the next step
-    T.queue[0] = 0u;  // item counters of the moments and apply kernels
-    T.queue[1] = 0u;
   }
+}
+
+// Split step: the group's summed {sum of raw g^2, inf/NaN count} -> the
+// step's scalars, exactly as the grad-norm kernel's last CTA forms them.
+__global__ void finalize_kernel(DevTables T, NormArgs na, ScaleArgs sa) {
+  if (threadIdx.x == 0) publish_step(T, na, sa, T.xn[0], !(T.xn[1] == 0.0));
+}
+
+// Split step: trust ratio of each tensor shared with other ranks, from the
+// group's summed {sum w^2, sum r^2} of its exchange slot.
+__global__ void exchange_trust_kernel(DevTables T) {
+  const int32_t i = int32_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= T.n_tensors || T.sc->skip) return;
+  const int32_t k = T.td[i].xslot;
+  if (k >= 0) T.trust[i] = trust_of(T.xt[2 * k], T.xt[2 * k + 1]);
 }
 
 // ================================================ B: moments + norms pass
@@ -506,17 +697,40 @@ __device__ __forceinline__ void apply_range(const TensorDesc& d, int64_t begin, 
   }
 }
 
+// The first bytes of a chunk item's g, m, v and w, prefetched into L2 by one
+// thread while the kernel waits for the grad-norm kernel to finish.
+constexpr int64_t kPrefetchElems = 4096;
+
+template <int DT>
+__device__ __forceinline__ void prefetch_item(const DevTables& T, int32_t it) {
+  const lamb_work_item wi = T.items[it];
+  if (wi.tensor < 0) return;
+  const TensorDesc d = T.td[wi.tensor];
+  const uint32_t n = uint32_t(min(int64_t(wi.count), kPrefetchElems) & ~int64_t(7));
+  prefetch_l2(static_cast<const uint16_t*>(T.grads[wi.tensor]) + wi.begin, n * 2u);
+  prefetch_l2(d.m + wi.begin, n * 4u);
+  prefetch_l2(d.v + wi.begin, n * 4u);
+  prefetch_l2(d.w + wi.begin, n * 4u);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(DevTables T, Hyper hp) {
   __shared__ double2 red[kWarps];
   __shared__ int is_last;
+  __shared__ int32_t slot;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Before the wait: take the first item (this step's counter was reset one
+  // step ago) and prefetch its first bytes; nothing the grad-norm kernel
+  // writes is read here.
+  ItemQueue q{&T.queue[hp.parity], T.n_items, &slot, int32_t(blockIdx.x)};
+  int32_t it = q.next();
+  if (threadIdx.x == 0 && it < T.n_items) prefetch_item<DT>(T, it);
+  pdl_wait();
+  pdl_trigger();  // the apply kernel may launch as this grid drains
   const StepScalars* sc = T.sc;
   if (sc->skip) return;
-  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, sc->gscale};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __shared__ int32_t slot;
-  ItemQueue q{&T.queue[0], T.n_items, &slot, int32_t(blockIdx.x)};
-  for (int32_t it = q.next(); it < T.n_items; it = q.next()) {
+  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, sc->c1, sc->c2, hp.eps, sc->gscale};
+  for (; it < T.n_items; it = q.next()) {
     const lamb_work_item wi = T.items[it];
     if (wi.tensor >= 0) {
       const TensorDesc d = T.td[wi.tensor];
@@ -525,7 +739,20 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
                         threadIdx.x, kThreads, e, sw, sr);
       const double2 s = block_sum2(sw, sr, red);
       if (d.n_items == 1) {
-        if (threadIdx.x == 0) T.trust[wi.tensor] = trust_of(s.x, s.y);
+        if (d.xslot >= 0) {  // shared with other ranks: out for summing
+          if (threadIdx.x == 0) {
+            T.xt[2 * d.xslot] = s.x;
+            T.xt[2 * d.xslot + 1] = s.y;
+          }
+          continue;
+        }
+        // A tensor of one item is finished here, in one pass: every thread
+        // re-reads only the elements it has just written or read itself (the
+        // same thread-to-element map in both loops), so the update reads
+        // cache, not HBM, and the apply kernel skips the item.
+        const float tr = trust_of(s.x, s.y);
+        if (threadIdx.x == 0) T.trust[wi.tensor] = tr;
+        apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, __fmul_rn(hp.lr, tr));
         continue;
       }
       if (threadIdx.x == 0) {
@@ -547,7 +774,12 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
         }
         const double2 tot = block_sum2(a, b, red);
         if (threadIdx.x == 0) {
-          T.trust[wi.tensor] = trust_of(tot.x, tot.y);
+          if (d.xslot >= 0) {  // shared with other ranks: out for summing
+            T.xt[2 * d.xslot] = tot.x;
+            T.xt[2 * d.xslot + 1] = tot.y;
+          } else {
+            T.trust[wi.tensor] = trust_of(tot.x, tot.y);
+          }
           T.tensor_ticket[wi.tensor] = 0u;
         }
       }
@@ -574,15 +806,18 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
 
 // ========================================================= C: apply pass
 __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTables T, Hyper hp) {
+  __shared__ int32_t slot;
+  ItemQueue q{&T.queue[2 + hp.parity], T.n_items, &slot, int32_t(blockIdx.x)};
+  int32_t it = q.next();  // before the wait: the counter was reset one step ago
+  pdl_wait();
   const StepScalars* sc = T.sc;
   if (sc->skip) return;
-  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, 0.0f};
-  __shared__ int32_t slot;
-  ItemQueue q{&T.queue[1], T.n_items, &slot, int32_t(blockIdx.x)};
-  for (int32_t it = q.next(); it < T.n_items; it = q.next()) {
+  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, sc->c1, sc->c2, hp.eps, 0.0f};
+  for (; it < T.n_items; it = q.next()) {
     const lamb_work_item wi = T.items[LAMB_REVERSE_C ? T.n_items - 1 - it : it];
     if (wi.tensor < 0) continue;  // packs were finished by the moments kernel
     const TensorDesc d = T.td[wi.tensor];
+    if (d.n_items == 1 && d.xslot < 0) continue;  // so were tensors of one item
     const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
     apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
   }
@@ -652,22 +887,25 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_tma_kernel(D
   extern __shared__ __align__(128) unsigned char tma_smem[];
   __shared__ __align__(8) uint64_t full[kTmaStages];
   __shared__ int32_t slot;
-  const StepScalars* sc = T.sc;
-  if (sc->skip) return;
-  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, hp.c1, hp.c2, hp.eps, 0.0f};
   float* stage_buf = reinterpret_cast<float*>(tma_smem);  // [stage][m|v|w][piece]
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTmaStages; ++s) mbar_init(&full[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  // Before the wait: take the first item (the counter was reset one step ago).
+  ItemQueue q{&T.queue[2 + hp.parity], T.n_items, &slot, int32_t(blockIdx.x)};
+  int32_t it = q.next();  // its __syncthreads also publishes the mbarrier init
+  pdl_wait();
+  const StepScalars* sc = T.sc;
+  if (sc->skip) return;
+  const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, sc->c1, sc->c2, hp.eps, 0.0f};
   uint32_t parity = 0;  // bit s: the phase to wait for on stage s
   bool ok = true;
-  ItemQueue q{&T.queue[1], T.n_items, &slot, int32_t(blockIdx.x)};
-  for (int32_t it = q.next(); it < T.n_items && ok; it = q.next()) {
+  for (; it < T.n_items && ok; it = q.next()) {
     const lamb_work_item wi = T.items[LAMB_REVERSE_C ? T.n_items - 1 - it : it];
-    if (wi.tensor < 0) continue;
+    if (wi.tensor < 0) continue;  // packs were finished by the moments kernel
     const TensorDesc d = T.td[wi.tensor];
+    if (d.n_items == 1 && d.xslot < 0) continue;  // so were tensors of one item
     const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
     const int64_t body = (int64_t(wi.count) >> 3) << 3;  // elements in whole vectors
     const int npieces = int((body + kTmaPiece - 1) / kTmaPiece);
@@ -691,6 +929,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_tma_kernel(D
         ok = false;
         if (threadIdx.x == 0) {
           atomicOr(reinterpret_cast<unsigned int*>(&T.sc->error), 1u);
+          if (hp.slot) static_cast<volatile ResultRecord*>(hp.slot)->error = 1;
           // Let the copies still in flight (pieces p .. p+stages-1) land,
           // again bounded, before leaving.
           for (int r = p; r < npieces && r < p + kTmaStages; ++r) {
@@ -730,6 +969,16 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_tma_kernel(D
     }
     if (ok) apply_range(d, wi.begin + body, wi.count - body, threadIdx.x, kThreads, e, step);
   }
+#ifdef LAMB_TEST_APPLY_REPORTS_WAIT_ERROR
+  // Test builds only: CTA 0 reports a given-up wait after finishing its work
+  // normally (no copy is in flight), so that the host's handling of the
+  // error can be tested without any wait actually running out.
+  __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    atomicOr(reinterpret_cast<unsigned int*>(&T.sc->error), 1u);
+    if (hp.slot) static_cast<volatile ResultRecord*>(hp.slot)->error = 1;
+  }
+#endif
 }
 #endif
 
@@ -767,32 +1016,75 @@ int max_blocks_per_sm(int kernel, int grad_dtype) {
   return nb < cap ? nb : cap;
 }
 
-int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, float clip,
+int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, const NormArgs& na,
                      const ScaleArgs& sa, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (grad_dtype == LAMB_GRAD_FP16)
-    grad_norm_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, clip, sa);
+    grad_norm_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, na, sa);
   else
-    grad_norm_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, clip, sa);
+    grad_norm_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, na, sa);
   return int(cudaGetLastError());
 }
 
-int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (grad_dtype == LAMB_GRAD_FP16)
-    moments_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, hp);
-  else
-    moments_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, hp);
+__global__ void set_step_kernel(StepScalars* sc, int64_t t, double p1, double p2) {
+  sc->t_next = t;
+  sc->p1_next = p1;
+  sc->p2_next = p2;
+}
+
+int launch_finalize(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, void* stream) {
+  finalize_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(T, na, sa);
   return int(cudaGetLastError());
+}
+
+int launch_exchange_trust(const DevTables& T, void* stream) {
+  const int blocks = T.n_tensors > 0 ? (T.n_tensors + kThreads - 1) / kThreads : 1;
+  exchange_trust_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(T);
+  return int(cudaGetLastError());
+}
+
+int launch_set_step(StepScalars* sc, int64_t t, double p1, double p2, void* stream) {
+  set_step_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(sc, t, p1, p2);
+  return int(cudaGetLastError());
+}
+
+namespace {
+// Launch configuration of a kernel that depends programmatically (PDL) on
+// the kernel before it in the stream.
+struct DependentLaunch {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  DependentLaunch(int grid, size_t smem, void* stream) {
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = LAMB_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+}  // namespace
+
+int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream) {
+  DependentLaunch L(grid, 0, stream);
+  const cudaError_t e =
+      grad_dtype == LAMB_GRAD_FP16
+          ? cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_FP16>, T, hp)
+          : cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_BF16>, T, hp);
+  return e != cudaSuccess ? int(e) : int(cudaGetLastError());
 }
 
 int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream) {
 #if LAMB_TMA_C
-  apply_tma_kernel<<<grid, kThreads, kTmaSmem, static_cast<cudaStream_t>(stream)>>>(T, hp);
+  DependentLaunch L(grid, kTmaSmem, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, apply_tma_kernel, T, hp);
 #else
-  apply_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(T, hp);
+  DependentLaunch L(grid, 0, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, apply_kernel, T, hp);
 #endif
-  return int(cudaGetLastError());
+  return e != cudaSuccess ? int(e) : int(cudaGetLastError());
 }
 
 }  // namespace lambgb

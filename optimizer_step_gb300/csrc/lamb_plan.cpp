@@ -30,8 +30,8 @@ int64_t choose_chunk(int64_t n_params, int64_t cta_slots) {
   return std::min(kChunkElems, std::max(kMinChunkElems, c));
 }
 
-bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems, Plan* plan,
-                std::string* err) {
+bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
+                const uint8_t* no_pack, Plan* plan, std::string* err) {
   plan->items.clear();
   plan->pack_ids.clear();
   plan->first_item.assign(size_t(std::max(n_tensors, 0)), -1);
@@ -65,7 +65,7 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems, Pl
       *err = "sizes[" + std::to_string(i) + "] is negative";
       return false;
     }
-    if (n == 0 || n > kSmallMax) continue;
+    if (n == 0 || n > kSmallMax || (no_pack && no_pack[i])) continue;
     if (pack_elems + n > pack_budget || int64_t(plan->pack_ids.size()) - pack_begin >= kPackMax)
       close_pack();
     plan->pack_ids.push_back(i);
@@ -73,10 +73,15 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems, Pl
   }
   close_pack();
 
-  // Then the chunks of every large tensor, each tensor's chunks contiguous.
+  // Then the chunks of every large tensor (and of every small one that must
+  // not be packed), each tensor's chunks contiguous: first the tensors of a
+  // single chunk (the moments kernel finishes them in one pass, a chain of
+  // latencies that should not trail at the end of the kernel), then the rest.
+  for (int pass = 0; pass < 2; ++pass)
   for (int32_t i = 0; i < n_tensors; ++i) {
     const int64_t n = sizes[i];
-    if (n <= kSmallMax) continue;
+    if (n == 0 || (n <= kSmallMax && !(no_pack && no_pack[i]))) continue;
+    if ((n <= chunk_elems) != (pass == 0)) continue;
     const int64_t nchunks = (n + chunk_elems - 1) / chunk_elems;
     int64_t per = (n + nchunks - 1) / nchunks;
     per = (per + 7) / 8 * 8;
@@ -109,7 +114,7 @@ LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_el
   lambgb::Plan plan;
   std::string err;
   if (chunk_elems == 0) chunk_elems = lambgb::kChunkElems;
-  if (!lambgb::build_plan(n_tensors, sizes, chunk_elems, &plan, &err)) {
+  if (!lambgb::build_plan(n_tensors, sizes, chunk_elems, nullptr, &plan, &err)) {
     lambgb::set_last_error(err);
     return LAMB_ERR_INVALID;
   }

@@ -40,6 +40,16 @@ def _check_tensors(name, tensors, dtype, sizes, device):
             raise ValueError(f"{name}[{i}]: must be contiguous with {n} elements")
 
 
+class GradSet:
+    """Grad tensors already checked against a handle, with their pointer array."""
+
+    __slots__ = ("tensors", "ptrs")
+
+    def __init__(self, tensors, ptrs):
+        self.tensors = tensors
+        self.ptrs = ptrs
+
+
 class Lamb:
     """LAMB optimizer state bound to caller-owned CUDA tensors.
 
@@ -48,13 +58,22 @@ class Lamb:
     per-tensor 0/1 (1 = apply weight decay).  All tensors must be contiguous,
     16-byte aligned and on one CUDA device.  ``stream`` defaults to the
     current torch stream at construction; every step runs on it.
+
+    For one rank of a data-parallel group whose shard boundaries cut tensors
+    (the split step, ``split_norms`` / ``split_moments`` / ``split_apply``):
+    ``norm_exchange`` is a float64 CUDA tensor of 2 elements and
+    ``tensor_exchange`` one of 2 * n_slots elements, both caller-owned, and
+    ``exchange_slots`` gives each tensor -1 (held whole) or its slot.
     """
 
     def __init__(self, weights: Sequence[torch.Tensor], exp_avg: Sequence[torch.Tensor],
                  exp_avg_sq: Sequence[torch.Tensor], weights_bf16: Sequence[torch.Tensor],
                  wd_flags: Sequence[int], *, beta1: float = 0.9, beta2: float = 0.999,
                  eps: float = 1e-6, weight_decay: float = 0.01,
-                 grad_dtype: torch.dtype = torch.bfloat16, stream=None):
+                 grad_dtype: torch.dtype = torch.bfloat16, stream=None,
+                 exchange_slots: Sequence[int] | None = None,
+                 norm_exchange: torch.Tensor | None = None,
+                 tensor_exchange: torch.Tensor | None = None):
         self._lib = _lib.load()
         self._h = None
         if grad_dtype not in _GRAD_CODES:
@@ -78,10 +97,37 @@ class Lamb:
             sizes = np.asarray(self.sizes, dtype=np.int64)
             flags = np.asarray([1 if f else 0 for f in wd_flags], dtype=np.uint8)
             h = ctypes.c_void_p()
-            check(self._lib.lamb_create(
-                ctypes.byref(h), n, sizes.ctypes.data, flags.ctypes.data, _ptrs(weights),
-                _ptrs(exp_avg), _ptrs(exp_avg_sq), _ptrs(weights_bf16), ctypes.byref(hp),
-                ctypes.c_void_p(self.stream.cuda_stream)))
+            if norm_exchange is None and tensor_exchange is None and exchange_slots is None:
+                check(self._lib.lamb_create(
+                    ctypes.byref(h), n, sizes.ctypes.data, flags.ctypes.data, _ptrs(weights),
+                    _ptrs(exp_avg), _ptrs(exp_avg_sq), _ptrs(weights_bf16), ctypes.byref(hp),
+                    ctypes.c_void_p(self.stream.cuda_stream)))
+            else:
+                slots = np.full(max(1, n), -1, dtype=np.int32)
+                if exchange_slots is not None:
+                    if len(exchange_slots) != n:
+                        raise ValueError("exchange_slots must have one entry per tensor")
+                    slots[:n] = np.asarray(exchange_slots, dtype=np.int32)
+                n_slots = 0
+                for name, x in (("norm_exchange", norm_exchange),
+                                ("tensor_exchange", tensor_exchange)):
+                    if x is not None and (x.dtype != torch.float64 or x.device != self.device
+                                          or not x.is_contiguous()):
+                        raise ValueError(f"{name}: need a contiguous float64 tensor on "
+                                         f"{self.device}")
+                if tensor_exchange is not None:
+                    if tensor_exchange.numel() % 2:
+                        raise ValueError("tensor_exchange: need 2 * n_slots elements")
+                    n_slots = tensor_exchange.numel() // 2
+                if norm_exchange is not None and norm_exchange.numel() != 2:
+                    raise ValueError("norm_exchange: need 2 elements")
+                self._exchange_keep = (norm_exchange, tensor_exchange)
+                ptr = lambda x: None if x is None else x.data_ptr()
+                check(self._lib.lamb_create_sharded(
+                    ctypes.byref(h), n, sizes.ctypes.data, flags.ctypes.data, _ptrs(weights),
+                    _ptrs(exp_avg), _ptrs(exp_avg_sq), _ptrs(weights_bf16), slots.ctypes.data,
+                    n_slots, ptr(norm_exchange), ptr(tensor_exchange), ctypes.byref(hp),
+                    ctypes.c_void_p(self.stream.cuda_stream)))
         self._h = h
         self._n = n
         self._grad_ptrs = None
@@ -91,11 +137,19 @@ class Lamb:
         self.next_loss_scale = None  # S the next step uses (dynamic scaling: for the backward)
 
     # ------------------------------------------------------------------ steps
-    def set_grads(self, grads: Sequence[torch.Tensor]) -> None:
-        """Validate and remember the grad tensors used by ``step()``."""
+    def prepare_grads(self, grads: Sequence[torch.Tensor]) -> "GradSet":
+        """Validate a list of grad tensors once and return it in a form that
+        ``set_grads`` / ``step`` / ``step_async`` take without checking again."""
         _check_tensors("grads", grads, self.grad_dtype, self.sizes, self.device)
-        self._grads_keep = list(grads)
-        self._grad_ptrs = _ptrs(grads)
+        return GradSet(list(grads), _ptrs(grads))
+
+    def set_grads(self, grads) -> None:
+        """Remember the grad tensors used by ``step()`` (a list of tensors, or
+        a ``GradSet`` from ``prepare_grads``)."""
+        if not isinstance(grads, GradSet):
+            grads = self.prepare_grads(grads)
+        self._grads_keep = grads.tensors
+        self._grad_ptrs = grads.ptrs
 
     def step(self, lr: float, t: int, clip: float = 0.0, loss_scale: float = 1.0,
              grads: Sequence[torch.Tensor] | None = None):
@@ -115,6 +169,73 @@ class Lamb:
         self.loss_scale = float(self._result.loss_scale)
         self.next_loss_scale = float(self._result.next_loss_scale)
         return bool(self._result.skipped), float(self._result.grad_norm)
+
+    def step_async(self, lr: float, clip: float = 0.0, loss_scale: float = 1.0,
+                   grads: Sequence[torch.Tensor] | None = None) -> int:
+        """Enqueue one LAMB step whose step number is the GPU's counter (see
+        ``set_step``); returns its sequence number at once, without waiting
+        for the GPU.  ``result(seq)`` gives its outcome."""
+        if self._h is None:
+            raise RuntimeError("handle is closed")
+        if grads is not None:
+            self.set_grads(grads)
+        if self._grad_ptrs is None:
+            raise ValueError("no grads: pass grads= or call set_grads first")
+        seq = ctypes.c_int64()
+        check(self._lib.lamb_step_async(self._h, self._grad_ptrs, float(lr), float(clip),
+                                        float(loss_scale), ctypes.byref(seq)))
+        return int(seq.value)
+
+    def result(self, seq: int, wait: bool = True):
+        """Outcome of step ``seq`` as ``(skipped, grad_norm, t)``, or ``None``
+        if ``wait`` is false and the step has not finished."""
+        res = LambResult()
+        rc = self._lib.lamb_step_result(self._h, int(seq), 1 if wait else 0, ctypes.byref(res))
+        if rc == _lib.LAMB_NOT_READY:
+            return None
+        check(rc)
+        self.loss_scale = float(res.loss_scale)
+        self.next_loss_scale = float(res.next_loss_scale)
+        return bool(res.skipped), float(res.grad_norm), int(res.t)
+
+    # ------------------------------------------------------------ split step
+    def split_norms(self, grads=None, loss_scale: float = 1.0) -> None:
+        """Phase 1 of a split step: this shard's grad-norm partials into
+        ``norm_exchange`` (sum them over the group before phase 2)."""
+        if grads is not None:
+            self.set_grads(grads)
+        if self._grad_ptrs is None:
+            raise ValueError("no grads: pass grads= or call set_grads first")
+        check(self._lib.lamb_split_norms(self._h, self._grad_ptrs, float(loss_scale)))
+
+    def split_moments(self, lr: float, clip: float = 0.0, t: int = 0) -> None:
+        """Phase 2: moments from the summed ``norm_exchange``; the shared
+        tensors' {sum w^2, sum r^2} into ``tensor_exchange`` (sum them over the
+        group before phase 3).  ``t`` 0: the GPU's step counter."""
+        check(self._lib.lamb_split_moments(self._h, float(lr), int(t), float(clip)))
+
+    def split_apply(self) -> int:
+        """Phase 3: the update from the summed ``tensor_exchange``; returns
+        the step's sequence number for ``result``."""
+        seq = ctypes.c_int64()
+        check(self._lib.lamb_split_apply(self._h, ctypes.byref(seq)))
+        return int(seq.value)
+
+    def one_pass_params(self) -> int:
+        """Elements whose whole step the moments kernel finishes (30 B/param)."""
+        n = ctypes.c_int64()
+        check(self._lib.lamb_one_pass_params(self._h, ctypes.byref(n)))
+        return int(n.value)
+
+    def set_step(self, t: int) -> None:
+        """Set the GPU's step counter: the t of the next ``step_async``."""
+        check(self._lib.lamb_set_step(self._h, int(t)))
+
+    def loss_scale_device_ptr(self) -> int:
+        """Device address of the dynamic loss scale (one fp32)."""
+        p = ctypes.c_void_p()
+        check(self._lib.lamb_loss_scale_device(self._h, ctypes.byref(p)))
+        return int(p.value)
 
     def set_loss_scaler(self, init_scale: float = 65536.0, growth_factor: float = 2.0,
                         backoff_factor: float = 0.5, growth_interval: int = 2000,
@@ -171,10 +292,14 @@ class Lamb:
         """Turn the library's CUDA event monitor on or off."""
         check(self._lib.lamb_set_timing(self._h, 1 if enable else 0))
 
-    def kernel_times(self):
-        """Device milliseconds of the last step's (grad-norm, moments, apply) kernels."""
+    def kernel_times(self, seq: int | None = None):
+        """Device milliseconds of the (grad-norm, moments, apply) kernels of
+        step ``seq`` (default: the last step enqueued)."""
         ms = (ctypes.c_float * 3)()
-        check(self._lib.lamb_kernel_times(self._h, ms))
+        if seq is None:
+            check(self._lib.lamb_kernel_times(self._h, ms))
+        else:
+            check(self._lib.lamb_step_kernel_times(self._h, int(seq), ms))
         return float(ms[0]), float(ms[1]), float(ms[2])
 
     def close(self) -> None:
@@ -225,4 +350,4 @@ def plan_limits() -> dict:
                     (v.value for v in vals)))
 
 
-__all__ = ["Lamb", "LambError", "plan", "plan_limits"]
+__all__ = ["Lamb", "GradSet", "LambError", "plan", "plan_limits"]

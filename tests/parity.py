@@ -154,3 +154,55 @@ def run_parity(wl: W.Workload, steps: int, check_steps: Iterable[int] = (),
     finally:
         opt.close()
     return log
+
+
+def run_parity_async(wl: W.Workload, phases: Sequence[int],
+                     subset: Optional[Sequence[int]] = None, device: str = "cuda") -> dict:
+    """Runs the GPU path with asynchronous steps (``step_async``: the step
+    number on the GPU, no host wait between steps) against the oracle.
+
+    ``phases`` lists step counts: each phase enqueues that many steps back to
+    back, every step with its own grad buffer filled beforehand, then waits
+    once, compares every step's outcome (skip flag, grad norm, the step number
+    the GPU used) with the oracle's, and the state of ``subset`` (all tensors
+    if None) at the end of the phase."""
+    st = W.make_state(wl, device)
+    hs = HostState(st, subset)
+    opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, beta1=wl.beta1, beta2=wl.beta2,
+               eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype)
+    opt.set_step(wl.t0)
+    t = wl.t0
+    k = 0
+    log = {"skipped": [], "bf16_mismatch": 0, "checked": 0, "t": []}
+    try:
+        for n_steps in phases:
+            bufs = []
+            for j in range(n_steps):
+                flat, views = W.grad_buffer(wl, device)
+                W.fill_grads(wl, k + j + 1, flat)
+                bufs.append((flat, views, opt.prepare_grads(views)))
+            torch.cuda.synchronize()
+            seqs = [opt.step_async(wl.lr, wl.clip, wl.loss_scale, grads=b[2]) for b in bufs]
+            outcomes = [opt.result(q) for q in seqs]
+            for (flat, views, _), (sk, gn, t_gpu) in zip(bufs, outcomes):
+                k += 1
+                g_host = [W.as_bits(x) for x in views]
+                osk, ogn, otrust = oracle_step(wl, hs, g_host, t)
+                assert int(sk) == osk, f"step {k}: skip {sk} vs oracle {osk}"
+                assert t_gpu == t, f"step {k}: the GPU used t={t_gpu}, the oracle t={t}"
+                log["skipped"].append(int(sk))
+                log["t"].append(t_gpu)
+                if osk:
+                    assert gn == math.inf
+                else:
+                    assert_close(np.array([gn]), np.array([ogn]), rtol_for(k),
+                                 f"step {k} grad_norm")
+                    t += 1
+            r = compare_state(st, hs, rtol_for(k), f"after step {k}", opt,
+                              None if osk else otrust)
+            log["bf16_mismatch"] += r["bf16_mismatch"]
+            log["checked"] += r["checked"]
+            del bufs
+    finally:
+        opt.close()
+    return log

@@ -73,9 +73,13 @@ def check_plan(sizes, chunk=0):
             assert b == at
             at += c
         assert at == sizes[t]
-    # chunk items of one tensor are contiguous in the table, tensors in order
+    # chunk items of one tensor are contiguous in the table; tensors of one
+    # chunk first, then the rest, each group in tensor order
     tens = [int(t) for t in items["tensor"] if t >= 0]
-    assert tens == sorted(tens)
+    single = [t for t in tens if len(counts[t]) == 1]
+    multi = [t for t in tens if len(counts[t]) > 1]
+    assert tens == single + multi
+    assert single == sorted(single) and multi == sorted(multi)
     first = {}
     for k, t in enumerate(tens):
         first.setdefault(t, k)

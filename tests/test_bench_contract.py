@@ -1,7 +1,7 @@
 """bench.py's command-line contract on a machine without a GPU.
 
-The reference arm times the CPU oracle on a bounded sample of the workload, so
-it runs here: one JSON line with the keys the contract fixes, and under a
+The reference arm times the CPU oracle on the host cores (here on a cut of
+the workload, every tensor at most 65,536 elements, so that it is quick): one JSON line with the keys the contract fixes, and under a
 two-rank launch only rank 0 prints.  The CUDA arm must refuse to run without
 a device rather than fall back to anything.
 """
@@ -52,7 +52,8 @@ def _check_reference_line(d, n_gpus, steps, warmup):
 
 
 def test_reference_arm_prints_one_contract_line():
-    r = _run(["bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3"])
+    r = _run(["bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
+              "--max-elems", "65536"])
     assert r.returncode == 0, r.stderr
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
@@ -64,7 +65,8 @@ def test_reference_arm_under_two_ranks_prints_once():
     env = dict(os.environ, MASTER_ADDR="127.0.0.1")
     r = _run(["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
               "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
-              "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"], env=env)
+              "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+              "--max-elems", "65536"], env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1

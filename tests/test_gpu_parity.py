@@ -10,7 +10,7 @@ import oracle
 import workloads as W
 from optimizer_step_gb300 import Lamb, LambError
 
-from parity import assert_close, check_bf16_copy, f32, run_parity
+from parity import assert_close, check_bf16_copy, f32, run_parity, run_parity_async
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +33,10 @@ SHAPES = {
     "several_tiles_ragged_tail": [5 * 32768 + 1234, 300001],
     "many_small": [int(x) for x in np.random.default_rng(3).integers(1, 300, 700)],
     "empty_mixed": [0, 17, 0, 40000, 0],
+    # one work item each (finished in one pass inside the moments kernel) up
+    # to the chunk size, several items above it; ragged tails throughout
+    "mid_sizes": [4097, 4103, 8191, 8200, 16385, 24577, 32767, 32768, 32769, 65535, 65543,
+                  100003, 131071, 131072],
 }
 
 
@@ -361,6 +365,47 @@ def test_config_fp16_twenty_steps_with_injected_overflow():
     log = run_parity(wl, 20, check_steps=(1, 6, 7, 8, 10, 15, 16, 20), subset=subset)
     want = [1 if k in (7, 15) else 0 for k in range(1, 21)]
     assert log["skipped"] == want
+
+
+def test_async_steps_fp16_twenty_with_injected_overflow():
+    """Twenty fp16 steps of the fp16 config's tensor mix (every tensor cut to
+    70,001 elements), enqueued asynchronously in phases of 6, 4 and 10 steps:
+    steps 7 and 15 carry an inf / a NaN, so the GPU's step counter must stay
+    put there.  Every outcome and the state after each phase match the oracle."""
+    wl = W.scaled(W.fp16_24(), 70001)
+    log = run_parity_async(wl, [6, 4, 10])
+    assert log["skipped"] == [1 if k in (7, 15) else 0 for k in range(1, 21)]
+    assert log["t"][-1] == 18  # t started at 1 and two steps were skipped
+
+
+def test_async_and_synchronous_steps_mix():
+    """lamb_step with an explicit t leaves the GPU counter at t+1 (clean) or
+    t (skipped), so asynchronous steps continue from there."""
+    wl = custom([5000, 70001, 17], t0=4, clip=0.5, inject={2: "inf"})
+    st = W.make_state(wl, "cuda")
+    opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags)
+    try:
+        _, gv = W.make_grads(wl, 1, "cuda")
+        assert opt.step(wl.lr, 9, wl.clip, 1.0, grads=gv)[0] is False
+        q = opt.step_async(wl.lr, wl.clip, 1.0)
+        assert opt.result(q)[2] == 10
+        _, gbad = W.make_grads(wl, 2, "cuda")
+        assert opt.step(wl.lr, 11, wl.clip, 1.0, grads=gbad)[0] is True
+        q = opt.step_async(wl.lr, wl.clip, 1.0, grads=gv)
+        assert opt.result(q)[2] == 11 and opt.result(q)[0] is False
+        opt.set_step(3)
+        q = opt.step_async(wl.lr, wl.clip, 1.0)
+        assert opt.result(q)[2] == 3
+        # Only the last 64 outcomes are kept; unknown sequence numbers are errors.
+        for _ in range(64):
+            last = opt.step_async(wl.lr, wl.clip, 1.0)
+        opt.result(last)
+        with pytest.raises(LambError):
+            opt.result(q)
+        with pytest.raises(LambError):
+            opt.result(last + 1)
+    finally:
+        opt.close()
 
 
 def test_config_ragged_full_step_then_ten_steps():

@@ -1,0 +1,205 @@
+"""The split step for a data-parallel (ZeRO-2) group whose shard boundaries
+cut tensors, against the oracle stepping the whole, unsplit shard.
+
+ZeRO-2 gives each data-parallel rank a contiguous slice of the flattened
+optimizer state (MegaScale guided-reading digest, section 3, "Data parallelism
+(ZeRO-2 style)"; the digest's "Terms" entry for ZeRO-2), so a rank's first and
+last tensors can be pieces of tensors other ranks also hold.  Each rank runs
+lamb_split_norms, the group sums the grad-norm partials, each runs
+lamb_split_moments, the group sums the shared tensors' {sum w^2, sum r^2}, and
+each runs lamb_split_apply.  Whatever the cut, the concatenated result must
+match one step of the whole shard.
+
+Here the ranks are handles on one GPU (their kernels never wait on one
+another; the sums go through host memory), and in the second test two
+processes on the same GPU that sum with a gloo all-reduce.  Runs of more than
+one GPU are not measured.
+"""
+import math
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from optimizer_step_gb300 import Lamb
+
+from parity import HostState, assert_close, compare_state, oracle_step, rtol_for
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [5000, 70001, 300, 200003, 17, 4096, 40000, 9]
+
+
+def _workload(inject=None, clip=0.02, grad_dtype=torch.bfloat16, S=1.0):
+    return W.Workload("split", "split", list(SIZES), [1, 1, 0, 1, 0, 0, 1, 0], [2],
+                      grad_dtype, t0=5, lr=1e-3, clip=clip, loss_scale=S, warm_state=True,
+                      grad_kind="normal", grad_sigma=1e-3, seed=77, inject=dict(inject or {}))
+
+
+def _rank_handle(wl, st, gviews, mine, slots, n_slots, device):
+    xn = torch.zeros(2, dtype=torch.float64, device=device)
+    xt = torch.zeros(max(2, 2 * n_slots), dtype=torch.float64, device=device)
+    take = lambda lst: [lst[i][b:e] for i, b, e in mine]
+    opt = Lamb(take(st.w), take(st.m), take(st.v), take(st.w16),
+               [wl.wd_flags[i] for i, _, _ in mine], grad_dtype=wl.grad_dtype,
+               exchange_slots=slots, norm_exchange=xn, tensor_exchange=xt)
+    return opt, xn, xt, opt.prepare_grads(take(gviews))
+
+
+def _split_step(ranks, wl, t, sum_fn):
+    """One split step over every rank; sum_fn sums a list of same-shaped
+    tensors (one per rank) and writes the sum back into each."""
+    for opt, xn, xt, g in ranks:
+        opt.split_norms(g, wl.loss_scale)
+    torch.cuda.synchronize()
+    sum_fn([r[1] for r in ranks])
+    for opt, xn, xt, g in ranks:
+        xt.zero_()
+        opt.split_moments(wl.lr, wl.clip, t)
+    torch.cuda.synchronize()
+    sum_fn([r[2] for r in ranks])
+    return [opt.split_apply() for opt, _, _, _ in ranks]
+
+
+def _host_sum(bufs):
+    total = sum(b.double().cpu() for b in bufs)
+    for b in bufs:
+        b.copy_(total)
+
+
+@pytest.mark.parametrize("n_ranks", [1, 2, 3, 5])
+def test_split_step_matches_the_whole_shard(n_ranks):
+    """n_ranks handles over the pieces of one shard, three steps (the second
+    carries an inf), t from the host then from the GPU's counter."""
+    wl = _workload(inject={2: "inf"})
+    st = W.make_state(wl, "cuda")
+    hs = HostState(st, None)
+    gflat, gviews = W.grad_buffer(wl, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, n_ranks)
+    n_slots = 1 + max([k for sl in slots for k in sl] + [-1])
+    ranks = [_rank_handle(wl, st, gviews, mine, sl, n_slots, "cuda")
+             for mine, sl in zip(pieces, slots)]
+    try:
+        t = wl.t0
+        for k in (1, 2, 3):
+            W.fill_grads(wl, k, gflat)
+            torch.cuda.synchronize()
+            g_host = [W.as_bits(x) for x in gviews]
+            seqs = _split_step(ranks, wl, t if k == 1 else 0, _host_sum)
+            if k == 1:
+                for opt, _, _, _ in ranks:
+                    opt.set_step(t + 1)  # later steps take the GPU's counter
+            outs = [opt.result(q) for (opt, _, _, _), q in zip(ranks, seqs)]
+            osk, ogn, otrust = oracle_step(wl, hs, g_host, t)
+            for sk, gn, t_used in outs:
+                assert int(sk) == osk and t_used == t
+                if osk:
+                    assert gn == math.inf
+                else:
+                    assert_close(np.array([gn]), np.array([ogn]), 1e-5, f"step {k} grad_norm")
+            if not osk:
+                t += 1
+            compare_state(st, hs, rtol_for(k), f"{n_ranks} ranks, step {k}")
+            if not osk:
+                for (opt, _, _, _), mine in zip(ranks, pieces):
+                    tr = opt.trust()
+                    want = np.array([otrust[i] for i, _, _ in mine])
+                    assert_close(tr, want, 1e-5, f"{n_ranks} ranks, step {k} trust")
+        assert [int(o[0]) for o in outs] == [0] * n_ranks
+    finally:
+        for opt, _, _, _ in ranks:
+            opt.close()
+
+
+def test_split_step_with_a_tensor_over_three_ranks_and_fp16_scale():
+    """One tensor cut across three ranks (the middle rank holds only a piece of
+    it), fp16 grads with a loss scale, clipping active."""
+    wl = W.Workload("split3", "split3", [3000, 300000, 5000], [1, 1, 0], [], torch.float16,
+                    t0=3, lr=1e-3, clip=1e-4, loss_scale=1024.0, warm_state=True,
+                    grad_kind="normal", grad_sigma=1e-3, seed=78)
+    st = W.make_state(wl, "cuda")
+    hs = HostState(st, None)
+    gflat, gviews = W.make_grads(wl, 1, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, 4)
+    assert pieces[1] == [(1, pieces[1][0][1], pieces[1][0][2])] and slots[1] == [0]
+    n_slots = 1
+    ranks = [_rank_handle(wl, st, gviews, mine, sl, n_slots, "cuda")
+             for mine, sl in zip(pieces, slots)]
+    try:
+        g_host = [W.as_bits(x) for x in gviews]
+        seqs = _split_step(ranks, wl, wl.t0, _host_sum)
+        osk, ogn, otrust = oracle_step(wl, hs, g_host, wl.t0)
+        assert osk == 0 and ogn * 1.0 > wl.clip  # clipping is active
+        for (opt, _, _, _), q in zip(ranks, seqs):
+            sk, gn, _ = opt.result(q)
+            assert sk is False
+            assert_close(np.array([gn]), np.array([ogn]), 1e-5, "grad_norm")
+        compare_state(st, hs, 1e-5, "three-rank tensor")
+    finally:
+        for opt, _, _, _ in ranks:
+            opt.close()
+
+
+# ------------------------------------------------ two processes, gloo sums
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, result_dir):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        torch.cuda.set_device(0)
+        wl = _workload(inject={2: "nan"})
+        st = W.make_state(wl, "cuda")  # every rank builds the same seeded shard
+        hs = HostState(st, None)
+        gflat, gviews = W.grad_buffer(wl, "cuda")
+        pieces, slots = W.zero2_pieces(wl.sizes, world)
+        n_slots = 1 + max([k for sl in slots for k in sl] + [-1])
+        ranks = [_rank_handle(wl, st, gviews, pieces[rank], slots[rank], n_slots, "cuda")]
+
+        def gloo_sum(bufs):
+            (b,) = bufs
+            h = b.cpu()
+            dist.all_reduce(h)
+            b.copy_(h)
+
+        t = wl.t0
+        skipped = []
+        for k in (1, 2, 3):
+            W.fill_grads(wl, k, gflat)
+            torch.cuda.synchronize()
+            g_host = [W.as_bits(x) for x in gviews]
+            (q,) = _split_step(ranks, wl, t, gloo_sum)
+            sk, gn, _ = ranks[0][0].result(q)
+            osk, ogn, _ = oracle_step(wl, hs, g_host, t)
+            assert int(sk) == osk
+            if not osk:
+                assert_close(np.array([gn]), np.array([ogn]), 1e-5, "grad_norm")
+                t += 1
+            skipped.append(int(sk))
+            # this rank's pieces against the oracle's whole tensors
+            for i, b, e in pieces[rank]:
+                for name, got, want in (("w", st.w, hs.w), ("m", st.m, hs.m), ("v", st.v, hs.v)):
+                    assert_close(W.as_f32(got[i][b:e]), want[i][b:e], rtol_for(k),
+                                 f"rank {rank} step {k} {name}[{i}][{b}:{e}]")
+        ranks[0][0].close()
+        with open(os.path.join(result_dir, f"rank{rank}.ok"), "w") as f:
+            f.write(" ".join(map(str, skipped)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_processes_sum_the_partials_with_gloo(tmp_path):
+    import torch.multiprocessing as mp
+    port = _free_port()
+    mp.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    for r in range(2):
+        assert (tmp_path / f"rank{r}.ok").read_text() == "0 1 0"

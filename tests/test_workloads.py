@@ -59,3 +59,26 @@ def test_student_t_has_heavy_tails():
     x = x[x != 0]
     kurt = np.mean(x ** 4) / np.mean(x ** 2) ** 2
     assert kurt > 6  # a normal has 3; t(3) has infinite kurtosis
+
+
+def test_zero2_pieces_cover_every_element_once_with_aligned_cuts():
+    sizes = [5000, 70001, 300, 200003, 17, 4096, 40000]
+    for n_ranks in (1, 2, 3, 5, 8):
+        pieces, slots = W.zero2_pieces(sizes, n_ranks)
+        seen = [np.zeros(n, np.int32) for n in sizes]
+        for mine, sl in zip(pieces, slots):
+            assert len(mine) == len(sl)
+            for (i, b, e), k in zip(mine, sl):
+                assert 0 <= b < e <= sizes[i]
+                assert b % 8 == 0  # every piece starts 16-byte aligned for 16-bit grads
+                seen[i][b:e] += 1
+                whole = b == 0 and e == sizes[i]
+                assert (k == -1) == whole
+        assert all((x == 1).all() for x in seen)
+        # the same shared tensor has the same slot on every rank
+        slot_of = {}
+        for mine, sl in zip(pieces, slots):
+            for (i, _, _), k in zip(mine, sl):
+                if k >= 0:
+                    assert slot_of.setdefault(i, k) == k
+        assert sorted(slot_of.values()) == list(range(len(slot_of)))

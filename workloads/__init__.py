@@ -292,3 +292,45 @@ def as_bits(t: torch.Tensor) -> np.ndarray:
 
 def as_f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().numpy().astype(np.float32, copy=False)
+
+
+# ------------------------------------------------------- ZeRO-2 rank pieces
+def zero2_pieces(sizes: Sequence[int], n_ranks: int, align: int = 8):
+    """Cut the concatenation of the tensors into ``n_ranks`` contiguous,
+    nearly equal shards, as ZeRO-2 shards a flattened model over its
+    data-parallel ranks; every cut is moved down to a multiple of ``align``
+    elements within the tensor it falls in (so each piece keeps 16-byte
+    alignment of 16-bit grads).
+
+    Returns ``(pieces, slots)``: ``pieces[r]`` lists rank r's ``(tensor,
+    begin, end)`` in order, and ``slots[r]`` gives each piece its exchange
+    slot: -1 if the rank holds the whole tensor, else the tensor's index among
+    the tensors that two or more ranks share (the same on every rank)."""
+    total = int(sum(sizes))
+    starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    cuts = [0]
+    for r in range(1, n_ranks):
+        c = (total * r) // n_ranks
+        ti = int(np.searchsorted(starts, c, side="right") - 1)
+        ti = min(ti, len(sizes) - 1)
+        local = c - int(starts[ti])
+        c = int(starts[ti]) + (local // align) * align
+        cuts.append(max(c, cuts[-1]))
+    cuts.append(total)
+    pieces = []
+    for r in range(n_ranks):
+        lo, hi = cuts[r], cuts[r + 1]
+        mine = []
+        for i, n in enumerate(sizes):
+            b, e = max(lo, int(starts[i])), min(hi, int(starts[i]) + int(n))
+            if b < e:
+                mine.append((i, b - int(starts[i]), e - int(starts[i])))
+        pieces.append(mine)
+    holders = {}
+    for r, mine in enumerate(pieces):
+        for i, b, e in mine:
+            holders.setdefault(i, set()).add(r)
+    shared = sorted(i for i, rs in holders.items() if len(rs) > 1)
+    slot_of = {i: k for k, i in enumerate(shared)}
+    slots = [[slot_of.get(i, -1) for i, _, _ in mine] for mine in pieces]
+    return pieces, slots
