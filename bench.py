@@ -11,8 +11,10 @@ Prints one JSON line on rank 0:
   value      params/s over all ranks with every input resident in HBM
   e2e        the same metric with each step's grads copied from pinned host
              memory inside the timed region (and the result read back)
-  roofline   the moments kernel (the largest of the three): algorithmic bytes
-             per launch / its CUDA-event duration against the measured HBM peak
+  roofline   the largest kernel (the persistent moments-and-apply kernel, or the
+             moments kernel when the two passes run as separate kernels):
+             algorithmic bytes per launch / its CUDA-event duration against
+             the measured HBM peak
   cpu_baseline  the CPU oracle timed on the host cores on a bounded sample
 
 ``--impl reference`` times the CPU oracle instead (on rank 0 only).
@@ -54,8 +56,19 @@ def kernel_bytes(n_params: int, n_packed: int) -> dict:
             for k in BYTES_PER_PARAM}
 
 
+def spec_kernel_bytes(n_params: int, n_packed: int, clipped: bool) -> dict:
+    """Speculative mode, one step: the one-pass kernel reads g, m, v, w and
+    writes the other set's m, v (22 B/param), then, if the step stands, reads
+    them back with w and writes w and the bf16 copy (18 B); a clipped step is
+    redone by the second kernel (an ordinary fused step without the grad norm:
+    40 B/param, 28 for one-pass tensors)."""
+    spec = 22 * n_params + (0 if clipped else 18 * n_params)
+    redo = (40 * (n_params - n_packed) + 28 * n_packed) if clipped else 0
+    return {"spec_step": spec, "redo": redo}
+
+
 FLOOR_BYTES_PER_PARAM = 28  # g read + w/m/v read and write + bf16 write
-RESULT_RECORD_BYTES = 40    # one step's outcome, written by the GPU into pinned host memory
+RESULT_RECORD_BYTES = 48    # one step's outcome, written by the GPU into pinned host memory
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCE = os.path.join(ROOT, "optimizer_step_gb300", "csrc", "lamb_kernels.cu")
@@ -75,6 +88,9 @@ def parse_args(argv=None):
     p.add_argument("--dynamic-loss-scale", action="store_true",
                    help="keep the loss scale on the GPU (lamb_set_loss_scaler) with the "
                         "workload's scale as the initial one")
+    p.add_argument("--speculative", action="store_true",
+                   help="speculative mode: a second set of m and v buffers, so that a step "
+                        "reads the grads once (40 B/param while no step is clipped)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--snapshot", action="store_true",
                    help="also time the state snapshot into pinned host memory (the first "
@@ -285,6 +301,9 @@ def run_ours(args, world, rank, local):
                eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype)
     grads0 = opt.prepare_grads(gv)
     opt.set_grads(grads0)
+    if args.speculative:
+        m2, v2 = torch.empty_like(st.m_flat), torch.empty_like(st.v_flat)
+        opt.set_speculative(st.views(m2), st.views(v2))
     if args.dynamic_loss_scale:
         opt.set_loss_scaler(init_scale=wl.loss_scale, growth_interval=2000)
     stream = opt.stream
@@ -318,7 +337,8 @@ def run_ours(args, world, rank, local):
     sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
     value = whole_job_rate(N, args.steps, world, sec)
     kept = seqs[-64:]  # the library keeps the last 64 steps' outcomes
-    skips = sum(int(opt.result(q)[0]) for q in kept)
+    outcomes = [opt.result(q) for q in kept]
+    skips = sum(int(o[0]) for o in outcomes)
 
     # ---- second timed region, the same steps with the event monitor on: the
     # per-kernel durations (events before and after each kernel, on the
@@ -331,21 +351,41 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     monitored_ms = e0.elapsed_time(e1) / args.steps
     ktimes = [opt.kernel_times(q) for q in seqs[-64:]]
-    skips += sum(int(opt.result(q)[0]) for q in seqs[-64:])
+    mon_outcomes = [opt.result(q) for q in seqs[-64:]]
+    skips += sum(int(o[0]) for o in mon_outcomes)
     opt.set_timing(False)
 
-    n_packed = opt.one_pass_params()
+    info = opt.info()
+    n_packed = info["one_pass_params"]
     kbytes = kernel_bytes(N, n_packed)
     step_bytes = sum(kbytes.values())
     kern = {}
-    for j, name in enumerate(("grad_norm", "moments", "apply")):
-        ms = statistics.mean(k[j] for k in ktimes)
+    times = {name: statistics.mean(k[j] for k in ktimes)
+             for j, name in enumerate(("grad_norm", "moments", "apply"))}
+    clipped_steps = 0
+    if info["speculative"]:
+        # Per-step bytes depend on whether the step was clipped (redone).
+        clip_of = lambda o: (not o[0]) and wl.clip > 0 and o[1] > wl.clip
+        per = [spec_kernel_bytes(N, n_packed, clip_of(o)) for o in mon_outcomes]
+        clipped_steps = sum(clip_of(o) for o in outcomes)
+        kbytes = {k: statistics.mean(p[k] for p in per) for k in ("spec_step", "redo")}
+        times = {"spec_step": times["moments"], "redo": times["apply"]}
+        step_bytes = statistics.mean(
+            sum(spec_kernel_bytes(N, n_packed, clip_of(o)).values()) for o in outcomes)
+    elif info["fused"]:
+        # One persistent kernel runs the moments and the apply passes.
+        kbytes = {"grad_norm": kbytes["grad_norm"],
+                  "moments_apply": kbytes["moments"] + kbytes["apply"]}
+        times = {"grad_norm": times["grad_norm"],
+                 "moments_apply": times["moments"] + times["apply"]}
+    for name, ms in times.items():
         gbs = kbytes[name] / (ms / 1e3) / 1e9 if ms > 0 else 0.0
         kern[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
                       "bytes_per_launch": kbytes[name]}
     peak, peak_kind = hbm_peak()
     step_ms = sec / args.steps * 1e3
-    dominant = "moments"
+    dominant = ("spec_step" if info["speculative"] else
+                "moments_apply" if info["fused"] else "moments")
     achieved = kern[dominant]["GB/s"]
     # The recorded counters come from a cut of the same tensor mix; they are
     # scaled by params only while one-pass tensors are a negligible share.
@@ -464,8 +504,11 @@ def run_ours(args, world, rank, local):
                                                  1e9, 1),
                          "floor_28B_frac_of_peak": round(FLOOR_BYTES_PER_PARAM * N /
                                                          (step_ms / 1e3) / 1e9 / peak, 4)},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (2 if info["fused"] or info["speculative"] else 3) * args.steps,
             "skipped_steps": skips,
+            "mode": ("speculative" if info["speculative"] else
+                     "fused" if info["fused"] else "three kernels"),
+            "clipped_steps": clipped_steps,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -302,11 +302,61 @@ LAMB_API int lamb_step_async(lamb_handle* h, const void* const* grads, float lr,
  */
 LAMB_API int lamb_step_result(lamb_handle* h, int64_t seq, int32_t wait, lamb_result* out);
 
-/* Number of elements the moments kernel finishes in one pass (packed small
- * tensors and tensors of a single work item, unless shared with other ranks):
- * their update re-reads the moments from cache, so they move 30 bytes per
- * element over HBM instead of 42. */
-LAMB_API int lamb_one_pass_params(lamb_handle* h, int64_t* n);
+/* What a handle was built with (for accounting and tests).
+ *   n_params         elements over all tensors
+ *   one_pass_params  elements the moments kernel finishes in one pass (packed
+ *                    small tensors and tensors of a single work item, unless
+ *                    shared with other ranks): their update re-reads the
+ *                    moments from cache, so they move 30 bytes per element
+ *                    over HBM instead of 42
+ *   chunk_elems      the chunk size of the work table
+ *   n_items          work items in the table
+ *   fused            1: an ordinary step runs the moments and apply passes as
+ *                    one persistent kernel (chosen when the work table holds
+ *                    at most 8 waves of items per resident CTA; the monitor
+ *                    then reports the apply kernel's time as 0); 0: as two
+ *                    kernels */
+typedef struct {
+  int64_t n_params;
+  int64_t one_pass_params;
+  int64_t chunk_elems;
+  int64_t n_items;
+  int32_t fused;
+  int32_t speculative;  /* 1 while speculative mode is on (lamb_set_speculative) */
+} lamb_info;
+LAMB_API int lamb_get_info(lamb_handle* h, lamb_info* out);
+
+/*
+ * Speculative mode (opt-in): a second, caller-owned set of m and v buffers
+ * lets a step read the grads once instead of twice.
+ *
+ *   m2[i], v2[i]  device pointers, n_i floats each, 16-byte aligned, distinct
+ *                 from every m and v; both arrays NULL turns the mode off
+ *
+ * In this mode one persistent kernel reads g, m, v and w, sums the grad norm
+ * on the way and writes the new m and v into the set the step did not start
+ * from, computed as if the step were neither skipped nor clipped; once the
+ * last moments item is done the grad norm is known, and the same kernel
+ * applies the update from the written set: 40 bytes per parameter over HBM
+ * instead of 42, and one kernel instead of two.  If the step turns out
+ * clipped, a second kernel redoes it from the untouched set (62 bytes per
+ * parameter for that step), so the mode pays only when clipping is rare or
+ * off.  A skipped step leaves the state where it was.  Results equal an
+ * ordinary step's bit for bit except the grad norm, which is summed in
+ * another order (within the parity tolerance).
+ *
+ * After a step that is not skipped the state (the current m and v) lives in
+ * the other set: lamb_state_buffers tells which.  lamb_snapshot_async copies
+ * the current set (it waits for the handle's stream to learn which).
+ * Turning the mode off (or switching to other buffers) first moves the state
+ * back into m and v.  Split steps and tensors with exchange slots are not
+ * supported in this mode (LAMB_ERR_INVALID).  The caller owns both sets.
+ */
+LAMB_API int lamb_set_speculative(lamb_handle* h, float* const* m2, float* const* v2);
+
+/* Speculative mode: *which = 0 if the state is in m, v, 1 if it is in m2, v2
+ * (waits for the handle's stream).  Always 0 when the mode is off. */
+LAMB_API int lamb_state_buffers(lamb_handle* h, int32_t* which);
 
 /* Sets the GPU's step counter (the t of the next lamb_step_async), t >= 1,
  * in stream order on the handle's stream. */

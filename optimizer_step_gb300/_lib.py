@@ -28,7 +28,7 @@ EXPORTS = ("lamb_create", "lamb_step", "lamb_destroy", "lamb_last_error", "lamb_
            "lamb_grad_norm_noalloc", "lamb_step_async", "lamb_step_result", "lamb_set_step",
            "lamb_loss_scale_device", "lamb_step_kernel_times", "lamb_create_sharded",
            "lamb_split_norms", "lamb_split_moments", "lamb_split_apply",
-           "lamb_one_pass_params")
+           "lamb_get_info", "lamb_set_speculative", "lamb_state_buffers")
 
 
 class LambHParams(ctypes.Structure):
@@ -46,6 +46,12 @@ class LambLossScaler(ctypes.Structure):
     _fields_ = [("init_scale", ctypes.c_float), ("growth_factor", ctypes.c_float),
                 ("backoff_factor", ctypes.c_float), ("growth_interval", ctypes.c_int32),
                 ("min_scale", ctypes.c_float), ("max_scale", ctypes.c_float)]
+
+
+class LambInfo(ctypes.Structure):
+    _fields_ = [("n_params", ctypes.c_int64), ("one_pass_params", ctypes.c_int64),
+                ("chunk_elems", ctypes.c_int64), ("n_items", ctypes.c_int64),
+                ("fused", ctypes.c_int32), ("speculative", ctypes.c_int32)]
 
 
 class LambWorkItem(ctypes.Structure):
@@ -91,8 +97,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.lamb_split_moments.argtypes = [P, f32, i64, f32]
         lib.lamb_split_apply.restype = ctypes.c_int
         lib.lamb_split_apply.argtypes = [P, ctypes.POINTER(i64)]
-        lib.lamb_one_pass_params.restype = ctypes.c_int
-        lib.lamb_one_pass_params.argtypes = [P, ctypes.POINTER(i64)]
+        lib.lamb_set_speculative.restype = ctypes.c_int
+        lib.lamb_set_speculative.argtypes = [P, P, P]
+        lib.lamb_state_buffers.restype = ctypes.c_int
+        lib.lamb_state_buffers.argtypes = [P, ctypes.POINTER(i32)]
+        lib.lamb_get_info.restype = ctypes.c_int
+        lib.lamb_get_info.argtypes = [P, ctypes.POINTER(LambInfo)]
         lib.lamb_step.restype = ctypes.c_int
         lib.lamb_step.argtypes = [P, P, f32, i64, f32, f32, ctypes.POINTER(LambResult)]
         lib.lamb_step_async.restype = ctypes.c_int

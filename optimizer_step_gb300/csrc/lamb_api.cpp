@@ -57,6 +57,18 @@ void lambgb::set_last_error(const std::string& msg) { g_last_error = msg; }
 // Steps whose outcome stays readable after they are enqueued (lamb_step_result).
 static constexpr int kResultRing = 64;
 
+// Ordinary steps run the moments and apply passes as one persistent kernel
+// when the work table holds at most this many waves of items (one item per
+// resident CTA), and as two kernels above that; 0 never fuses.  On GB300 the
+// fused kernel took 10% off a 16.8 M-param step and 3% off a 67 M-param one
+// (2 and 4.5 waves), tied on the 1.8 B-param shard and was 0.9% slower on the
+// 4,000-tensor ragged shard (73 waves), where the separate apply kernel's
+// staged copies and its walk from the table's end pay more.  Split steps
+// always use two kernels, with the exchange between them.
+#ifndef LAMB_FUSED_MAX_WAVES
+#define LAMB_FUSED_MAX_WAVES 8
+#endif
+
 struct lamb_handle {
   int device = 0;
   cudaStream_t stream = nullptr;
@@ -70,6 +82,9 @@ struct lamb_handle {
   cudaEvent_t ring_ev[kResultRing] = {};  // recorded after each step's last kernel
   int64_t next_seq = 0;            // sequence number of the next step
   int32_t split_a = 1;             // grad-norm sub-items per chunk item
+  int64_t chunk = 0;               // chunk size of the work table
+  bool fused = false;              // ordinary steps: moments and apply in one kernel
+  bool spec = false;               // speculative mode: second m, v buffers given
   int split_phase = 0;             // split step: 0 none, 1 norms enqueued, 2 moments enqueued
   float split_scale = 1.0f;        // split step: the fixed loss scale of phase 1
   float split_lr = 0.0f;           // split step: the learning rate of phase 2
@@ -186,6 +201,7 @@ Hyper make_hyper(const lamb_handle* h, float lr, int64_t seq) {
   hy.lr = lr;
   hy.slot = h->ring_dev + seq % kResultRing;
   hy.parity = int32_t(seq & 1);
+  hy.tag = uint32_t(seq % 0xFFFFFFFEll) + 1u;
   return hy;
 }
 
@@ -231,15 +247,29 @@ int enqueue_step(lamb_handle* h, const void* const* grads, float lr, int64_t t_h
   if ((ce = mark(h, r, 0)) != cudaSuccess) return cuda_fail(ce, "event record");
   ScaleArgs sa = h->scaler;
   sa.fixed = loss_scale;
+  if (h->spec) {
+    // One pass that also sums the grad norm, then the redo of a clipped step
+    // (which returns at once otherwise).
+    if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
+    if ((ce = mark(h, r, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
+    rc = launch_spec_step(h->T, h->grid[1], h->hp.grad_dtype, hy, na, sa, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "speculative step kernel launch");
+    if ((ce = mark(h, r, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
+    rc = launch_spec_redo(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "redo kernel launch");
+  } else {
   rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, na, sa, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
   if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
   if ((ce = mark(h, r, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
+  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->fused, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
   if ((ce = mark(h, r, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_apply(h->T, h->grid[2], hy, h->stream);
-  if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+  if (!h->fused) {
+    rc = launch_apply(h->T, h->grid[2], hy, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+  }
+  }
   if ((ce = mark(h, r, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
   if ((ce = cudaEventRecord(h->ring_ev[r], h->stream)) != cudaSuccess)
     return cuda_fail(ce, "event record");
@@ -247,6 +277,26 @@ int enqueue_step(lamb_handle* h, const void* const* grads, float lr, int64_t t_h
   if (h->timing && h->timed_from < 0) h->timed_from = seq;
   *seq_out = seq;
   return LAMB_OK;
+}
+
+// Speculative mode: waits for the handle's stream and reads which buffer set
+// (0: m, v; 1: the second set) holds the state.
+int current_set(lamb_handle* h, int32_t* cur) {
+  cudaError_t ce = cudaStreamSynchronize(h->stream);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpy(cur, reinterpret_cast<char*>(h->T.sc) + offsetof(StepScalars, cur),
+                    sizeof(int32_t), cudaMemcpyDeviceToHost);
+  return ce == cudaSuccess ? LAMB_OK : cuda_fail(ce, "reading which buffer set holds the state");
+}
+
+// Uploads the per-tensor records (after a change of the second buffer set).
+int upload_tensor_descs(lamb_handle* h) {
+  if (h->td_host.empty()) return LAMB_OK;
+  cudaError_t ce = cudaMemcpyAsync(const_cast<TensorDesc*>(h->T.td), h->td_host.data(),
+                                   h->td_host.size() * sizeof(TensorDesc),
+                                   cudaMemcpyHostToDevice, h->stream);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(h->stream);
+  return ce == cudaSuccess ? LAMB_OK : cuda_fail(ce, "uploading the tensor records");
 }
 
 // Copies a finished step's outcome out of its ring slot.
@@ -349,6 +399,7 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
     return fail(LAMB_ERR_INVALID, err);
   }
   h->n_tensors = n_tensors;
+  h->chunk = chunk;
   h->hp = *hp;
   h->stream = static_cast<cudaStream_t>(stream);
   h->sizes.assign(sizes, sizes + n_tensors);
@@ -367,6 +418,8 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
     td[i].first_item = h->plan.first_item[i];
     td[i].n_items = h->plan.n_items[i];
     td[i].xslot = exchange_slot ? exchange_slot[i] : -1;
+    td[i].m2 = nullptr;
+    td[i].v2 = nullptr;
   }
   std::vector<float> ones(nt, 1.0f);
   h->td_host = td;
@@ -387,8 +440,10 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
   const size_t o_wr = carve(ni * sizeof(double2));
   const size_t o_ticket = carve(nt * sizeof(uint32_t));
   const size_t o_trust = carve(nt * sizeof(float));
+  const size_t o_trust_spec = carve(nt * sizeof(float));
   const size_t o_sc = carve(sizeof(StepScalars));
   const size_t o_queue = carve(4 * sizeof(uint32_t));
+  const size_t o_ready = carve(nt * sizeof(uint32_t));
   ce = cudaMalloc(&h->dev_block, off);
   if (ce != cudaSuccess) {
     delete h;
@@ -422,8 +477,10 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
   T.item_wr = reinterpret_cast<double2*>(base + o_wr);
   T.tensor_ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
   T.trust = reinterpret_cast<float*>(base + o_trust);
+  T.trust_spec = reinterpret_cast<float*>(base + o_trust_spec);
   T.sc = reinterpret_cast<StepScalars*>(base + o_sc);
   T.queue = reinterpret_cast<uint32_t*>(base + o_queue);
+  T.ready = reinterpret_cast<uint32_t*>(base + o_ready);
   T.xn = norm_exchange;
   T.xt = tensor_exchange;
   T.n_items = int32_t(ni);
@@ -455,6 +512,7 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
     const int64_t full = int64_t(per_sm[k]) * sms;
     h->grid[k] = int(std::max<int64_t>(1, std::min<int64_t>(full, int64_t(ni))));
   }
+  h->fused = int64_t(ni) <= int64_t(LAMB_FUSED_MAX_WAVES) * h->grid[1] && ni > 0;
   // Sub-items per chunk item for the grad-norm kernel: about kSplitTarget per
   // CTA of its full grid, sub-items of at least kMinSubItem elements.
   {
@@ -542,6 +600,7 @@ LAMB_API int lamb_split_norms(lamb_handle* h, const void* const* grads, float lo
     return fail(LAMB_ERR_INVALID, "no norm exchange buffer: create the handle with "
                                   "lamb_create_sharded");
   if (h->split_phase != 0) return fail(LAMB_ERR_INVALID, "a split step is already in progress");
+  if (h->spec) return fail(LAMB_ERR_INVALID, "split steps do not run in speculative mode");
   int rc = LAMB_OK;
   if (!check_step_args(h, grads, 0.0f, 0.0f, loss_scale, &rc)) return rc;
   DeviceGuard dg(h->device);
@@ -579,7 +638,8 @@ LAMB_API int lamb_split_moments(lamb_handle* h, float lr, int64_t t, float clip)
   if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
   cudaError_t ce = mark(h, r, 1);
   if (ce != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, make_hyper(h, lr, seq), h->stream);
+  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, make_hyper(h, lr, seq), false,
+                      h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
   h->split_lr = lr;
   h->split_phase = 2;
@@ -610,14 +670,93 @@ LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq_out) {
   return LAMB_OK;
 }
 
-LAMB_API int lamb_one_pass_params(lamb_handle* h, int64_t* n) {
+LAMB_API int lamb_get_info(lamb_handle* h, lamb_info* out) {
   g_last_error.clear();
-  if (!h || !n) return fail(LAMB_ERR_INVALID, "NULL argument");
-  int64_t total = 0;
-  for (const TensorDesc& d : h->td_host)
-    if (d.n > 0 && d.xslot < 0 && (d.n_items == 0 || d.n_items == 1)) total += d.n;
-  *n = total;
+  if (!h || !out) return fail(LAMB_ERR_INVALID, "NULL argument");
+  std::memset(out, 0, sizeof *out);
+  for (const TensorDesc& d : h->td_host) {
+    out->n_params += d.n;
+    if (d.n > 0 && d.xslot < 0 && (d.n_items == 0 || d.n_items == 1)) out->one_pass_params += d.n;
+  }
+  out->chunk_elems = h->chunk;
+  out->n_items = int64_t(h->plan.items.size());
+  out->fused = h->fused ? 1 : 0;
+  out->speculative = h->spec ? 1 : 0;
   return LAMB_OK;
+}
+
+LAMB_API int lamb_set_speculative(lamb_handle* h, float* const* m2, float* const* v2) {
+  g_last_error.clear();
+  if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  if (h->split_phase != 0) return fail(LAMB_ERR_INVALID, "a split step is in progress");
+  const bool on = m2 || v2;
+  if (on && h->n_tensors > 0 && (!m2 || !v2))
+    return fail(LAMB_ERR_INVALID, "give both m2 and v2, or neither");
+  if (on) {
+    for (int32_t i = 0; i < h->n_tensors; ++i) {
+      const TensorDesc& d = h->td_host[size_t(i)];
+      if (d.xslot >= 0)
+        return fail(LAMB_ERR_INVALID, "speculative mode does not take tensors shared with other "
+                                      "ranks (split steps)");
+      if (d.n == 0) continue;
+      if (!m2[i] || !v2[i])
+        return fail(LAMB_ERR_INVALID, "tensor " + std::to_string(i) + " has a NULL m2 or v2");
+      if (!aligned16(m2[i]) || !aligned16(v2[i]))
+        return fail(LAMB_ERR_ALIGN,
+                    "tensor " + std::to_string(i) + " has an m2 or v2 not 16-byte aligned");
+      if (m2[i] == d.m || m2[i] == d.v || v2[i] == d.m || v2[i] == d.v || m2[i] == v2[i])
+        return fail(LAMB_ERR_INVALID,
+                    "tensor " + std::to_string(i) + ": m2 and v2 must be buffers of their own");
+    }
+  }
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  if (h->spec) {
+    // Bring the state back into m and v if it lives in the second set.
+    int32_t cur = 0;
+    int rc = current_set(h, &cur);
+    if (rc != LAMB_OK) return rc;
+    if (cur) {
+      cudaError_t ce = cudaSuccess;
+      for (const TensorDesc& d : h->td_host) {
+        if (d.n == 0) continue;
+        const size_t bytes = size_t(d.n) * sizeof(float);
+        if ((ce = cudaMemcpyAsync(d.m, d.m2, bytes, cudaMemcpyDeviceToDevice, h->stream)) !=
+                cudaSuccess ||
+            (ce = cudaMemcpyAsync(d.v, d.v2, bytes, cudaMemcpyDeviceToDevice, h->stream)) !=
+                cudaSuccess)
+          return cuda_fail(ce, "moving the state back into m and v");
+      }
+    }
+    for (TensorDesc& d : h->td_host) d.m2 = d.v2 = nullptr;
+    h->spec = false;
+  }
+  if (on) {
+    for (int32_t i = 0; i < h->n_tensors; ++i) {
+      h->td_host[size_t(i)].m2 = m2[i];
+      h->td_host[size_t(i)].v2 = v2[i];
+    }
+  }
+  const int krc = launch_set_cur(h->T.sc, 0, h->stream);
+  if (krc) return cuda_fail(cudaError_t(krc), "resetting the buffer set");
+  int rc = upload_tensor_descs(h);
+  if (rc != LAMB_OK) return rc;
+  h->spec = on && !h->plan.items.empty();
+  if (on && !h->spec) {  // an empty shard has nothing to speculate on
+    for (TensorDesc& d : h->td_host) d.m2 = d.v2 = nullptr;
+    return upload_tensor_descs(h);
+  }
+  return LAMB_OK;
+}
+
+LAMB_API int lamb_state_buffers(lamb_handle* h, int32_t* which) {
+  g_last_error.clear();
+  if (!h || !which) return fail(LAMB_ERR_INVALID, "NULL argument");
+  *which = 0;
+  if (!h->spec) return LAMB_OK;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
+  return current_set(h, which);
 }
 
 LAMB_API int lamb_set_step(lamb_handle* h, int64_t t) {
@@ -752,13 +891,20 @@ LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* co
   // that snap_done below covers every outstanding copy.
   if (h->snap_pending && (ce = cudaStreamWaitEvent(cs, h->snap_done, 0)) != cudaSuccess)
     return cuda_fail(ce, "ordering after the previous snapshot");
+  int32_t cur = 0;  // speculative mode: the set holding the state (the host waits to learn it)
+  if (h->spec) {
+    int rc = current_set(h, &cur);
+    if (rc != LAMB_OK) return rc;
+  }
   for (int32_t i = 0; i < h->n_tensors; ++i) {
     const TensorDesc& d = h->td_host[size_t(i)];
     if (d.n == 0) continue;
     const size_t bytes = size_t(d.n) * sizeof(float);
+    const float* m = cur ? d.m2 : d.m;
+    const float* v = cur ? d.v2 : d.v;
     if ((ce = cudaMemcpyAsync(host_w[i], d.w, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess ||
-        (ce = cudaMemcpyAsync(host_m[i], d.m, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess ||
-        (ce = cudaMemcpyAsync(host_v[i], d.v, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
+        (ce = cudaMemcpyAsync(host_m[i], m, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess ||
+        (ce = cudaMemcpyAsync(host_v[i], v, bytes, cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
       return cuda_fail(ce, "enqueueing snapshot copies");
   }
   if ((ce = cudaEventRecord(h->snap_done, cs)) != cudaSuccess)

@@ -55,6 +55,8 @@ struct TensorDesc {
   float* m;
   float* v;
   uint16_t* w16;
+  float* m2;           // speculative mode: the second m and v buffers (else NULL)
+  float* v2;
   int64_t n;
   float wd;            // weight_decay if the tensor's flag is set, else 0
   int32_t first_item;  // first chunk item of a chunked tensor
@@ -79,6 +81,14 @@ struct StepScalars {
   int64_t t_next;      // the step number of the next step (advances on clean steps)
   double p1_next;      // beta1^t_next and beta2^t_next (fp64; the host's pow when t
   double p2_next;      //   is set, then one multiplication per step that is not skipped)
+  // Speculative mode (second m and v buffers):
+  int32_t cur;         // which buffer set holds the state between steps (0: m, v; 1: m2, v2)
+  int32_t src;         // the set this step read (the update went to the other one)
+  int32_t spec_ok;     // 1: the step was neither skipped nor clipped: the speculative
+                       //    moments stand and the apply items of the same kernel run
+  uint32_t items_done; // moments items of the speculative kernel finished this step
+  uint32_t published;  // tag of the last step whose scalars are published
+  uint32_t pad;
 };
 
 // The outcome of one step as the host reads it: written by the GPU straight
@@ -90,6 +100,8 @@ struct ResultRecord {
   int64_t t_used;
   float scale_used;
   float scale_next;
+  int32_t state_buf;    // speculative mode: the buffer set holding the state after the step
+  int32_t pad;
   int32_t skipped;
   int32_t error;
 };
@@ -123,11 +135,14 @@ struct DevTables {
   double* item_g2;           // per CTA of the grad-norm kernel: sum of raw g^2
   double2* item_wr;          // per chunk item: (sum w^2, sum r^2)
   uint32_t* tensor_ticket;   // per tensor: chunk items finished this step
-  float* trust;              // per tensor: trust ratio of this step
+  float* trust;              // per tensor: trust ratio of the last step that was not skipped
+  float* trust_spec;         // speculative mode: per tensor, this step's trust ratio before the
+                             //   step is known to stand (copied into trust if it does)
   StepScalars* sc;
   uint32_t* queue;           // [4] item counters: moments [parity], apply [2 + parity]
   double* xn;                // split step: {sum of raw g^2, inf/NaN flag} (caller-owned)
   double* xt;                // split step: {sum w^2, sum r^2} per exchange slot (caller-owned)
+  uint32_t* ready;           // per tensor: tag of the step whose trust ratio is published
   int32_t n_items;
   int32_t n_tensors;
 };
@@ -137,6 +152,7 @@ struct Hyper {
   float eps, lr;
   ResultRecord* slot;        // device view of this step's result slot
   int32_t parity;            // this step's sequence number & 1: which item counters it uses
+  uint32_t tag;              // non-zero, different for consecutive steps: trust-ready flags
 };
 
 // Sets the calling thread's message returned by lamb_last_error().
@@ -156,7 +172,19 @@ int launch_set_step(StepScalars* sc, int64_t t, double p1, double p2, void* stre
 int launch_finalize(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, void* stream);
 // Split step: trust ratios of exchanged tensors from the group's summed xt.
 int launch_exchange_trust(const DevTables& T, void* stream);
-int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream);
+// fused: one persistent kernel takes the apply items too (ordinary steps).
+int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, bool fused,
+                   void* stream);
+// Speculative mode: the step's one pass (moments into the other buffer set
+// with the grad norm summed on the way, then the update if the step is
+// neither skipped nor clipped), and the redo of a clipped step (moments from
+// the untouched set with the clip factor, then the update; returns at once
+// otherwise).  Both launch with the grid of the moments kernel.
+int launch_spec_step(const DevTables& T, int grid, int grad_dtype, const Hyper& hp,
+                     const NormArgs& na, const ScaleArgs& sa, void* stream);
+int launch_spec_redo(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream);
+// Sets StepScalars::cur on the stream (speculative mode on or off).
+int launch_set_cur(StepScalars* sc, int32_t cur, void* stream);
 int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream);
 
 // Writes n grad pointers into the device array dst on the stream, by kernel

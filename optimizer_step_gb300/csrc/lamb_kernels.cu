@@ -201,6 +201,48 @@ __device__ __forceinline__ uint32_t nonfinite2(uint32_t x) {
   return uint32_t((u & 0xFFFFu) == 0u) | uint32_t((u >> 16) == 0u);
 }
 
+// Squares of grads.  A bf16 grad spans fp32's exponent range, so its square
+// can underflow (|g| below about 1e-19) or, summed with others, overflow
+// (|g| from about 1e18) in fp32.  Grads are squared in fp32 a few vectors at
+// a time; a partial that is not in [2^-90, 2^120] (while some grad of it is
+// not zero) is recomputed in fp64 on a separate, rare path.  Inside that
+// range nothing overflowed, and squares that underflowed weigh at most
+// 2^-30 of the partial.  fp16 squares are always normal fp32 numbers, so
+// fp16 grads never take the fp64 path.  (Choosing per pair instead, with
+// fp64 code inline, let the compiler predicate that code into every pair,
+// which made the grad-norm kernel twelve times slower on GB300.)
+template <int DT>
+__device__ __forceinline__ bool partial_out_of_range(float acc, uint32_t any_bits) {
+  if (DT != LAMB_GRAD_BF16) return false;
+  return !(acc <= 0x1p120f && (acc >= 0x1p-90f || (any_bits & 0x7FFF7FFFu) == 0u));
+}
+
+// The squares of the eight grads in four words, in fp64 (the rare path; not
+// inlined, and given the words by value, so that the fast path keeps its
+// words in registers and carries no fp64 code).
+template <int DT>
+__device__ __noinline__ double squares8_fp64(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  const uint32_t w[4] = {a, b, c, d};
+  double t = 0.0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = decode2<DT>(w[i]);
+    t = fma(double(f.x), double(f.x), t);
+    t = fma(double(f.y), double(f.y), t);
+  }
+  return t;
+}
+
+// The same for 4 * K words of a trip (K vectors).
+template <int DT, int K>
+__device__ __forceinline__ double trip_squares_fp64(const uint32_t (&w)[4 * K]) {
+  double t = 0.0;
+#pragma unroll
+  for (int u = 0; u < K; ++u)
+    t += squares8_fp64<DT>(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+  return t;
+}
+
 // -------------------------------------------------------------- reductions
 __device__ __forceinline__ double warp_sum(double x) {
 #pragma unroll
@@ -309,33 +351,36 @@ template <int DT>
 __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int64_t n, int tid,
                                             int nthr, double& total, uint32_t& bad) {
   const int64_t nv = n >> 3;
-  float acc = 0.0f;
   for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kLoadsA) * nthr) {
-    uint4 q[kLoadsA];
+    uint32_t w[4 * kLoadsA];
 #pragma unroll
     for (int u = 0; u < kLoadsA; ++u) {
       const int64_t k = k0 + int64_t(u) * nthr;
-      q[u] = k < nv ? ld_u4(g + 8 * k) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 q = k < nv ? ld_u4(g + 8 * k) : make_uint4(0u, 0u, 0u, 0u);
+      w[4 * u] = q.x;
+      w[4 * u + 1] = q.y;
+      w[4 * u + 2] = q.z;
+      w[4 * u + 3] = q.w;
     }
+    float acc = 0.0f;
+    uint32_t any = 0;
 #pragma unroll
-    for (int u = 0; u < kLoadsA; ++u) {
-      const uint32_t wv[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = decode2<DT>(wv[j]);
-        acc = __fmaf_rn(f.x, f.x, acc);
-        acc = __fmaf_rn(f.y, f.y, acc);
-        bad |= nonfinite2<DT>(wv[j]);
-      }
+    for (int j = 0; j < 4 * kLoadsA; ++j) {
+      const float2 f = decode2<DT>(w[j]);
+      acc = __fmaf_rn(f.x, f.x, acc);
+      acc = __fmaf_rn(f.y, f.y, acc);
+      any |= w[j];
+      bad |= nonfinite2<DT>(w[j]);
     }
+    total += partial_out_of_range<DT>(acc, any) ? trip_squares_fp64<DT, kLoadsA>(w)
+                                                : double(acc);
   }
-  for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {
+  for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {  // fewer than 8: fp64 squares
     const uint16_t x = g[j];
-    const float f = decode1<DT>(x);
-    acc = __fmaf_rn(f, f, acc);
+    const double f = double(decode1<DT>(x));
+    total = fma(f, f, total);
     bad |= nonfinite2<DT>(uint32_t(x) | (uint32_t(x) << 16));
   }
-  total += double(acc);
 }
 
 // Publishes one step's scalars from the sum of raw g^2 over the shard (or the
@@ -345,18 +390,20 @@ __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int6
 // that is not skipped -- fp64 is slow on GB300, so there is no pow here), the
 // dynamic loss scale, the host's copy of the outcome, and the item counters
 // of the next step.  One thread.
-__device__ void publish_step(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, double s,
+__device__ bool publish_step(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, double s,
                              bool nf) {
   StepScalars* sc = T.sc;
   const float S = sa.dynamic ? sc->scale : sa.fixed;
   const double loss_scale = double(S);
+  bool clipped = false;
   if (nf) {
     sc->skip = 1;
     sc->grad_norm = __longlong_as_double(0x7FF0000000000000ll);  // +inf
     sc->gscale = 0.0f;
   } else {
     const double gn = sqrt(s) / loss_scale;
-    const double c = (na.clip > 0.0f && gn > double(na.clip)) ? double(na.clip) / gn : 1.0;
+    clipped = na.clip > 0.0f && gn > double(na.clip);
+    const double c = clipped ? double(na.clip) / gn : 1.0;
     sc->skip = 0;
     sc->grad_norm = gn;
     sc->gscale = float(c / loss_scale);
@@ -402,6 +449,7 @@ __device__ void publish_step(const DevTables& T, const NormArgs& na, const Scale
   // take items before the kernel that publishes the step has finished).
   T.queue[1 - na.parity] = 0u;
   T.queue[3 - na.parity] = 0u;
+  return clipped;
 }
 
 // Each chunk item is cut into na.split equal sub-items (8-element aligned)
@@ -480,10 +528,11 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
     int64_t jbeg = 0, jend = s_vend[0];
     const uint4* jg = reinterpret_cast<const uint4*>(s_g[0]);
     for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += int64_t(kLoadsA) * kThreads) {
-      uint4 q[kLoadsA];
+      uint32_t w[4 * kLoadsA];
 #pragma unroll
       for (int u = 0; u < kLoadsA; ++u) {
         const int64_t v = v0 + int64_t(u) * kThreads;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
         if (v < nvec) {
           while (v >= jend) {
             ++j;
@@ -491,37 +540,37 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
             jend = s_vend[j];
             jg = reinterpret_cast<const uint4*>(s_g[j]);
           }
-          q[u] = ld_policy(jg + (v - jbeg));
-        } else {
-          q[u] = make_uint4(0u, 0u, 0u, 0u);
+          q = ld_policy(jg + (v - jbeg));
         }
+        w[4 * u] = q.x;
+        w[4 * u + 1] = q.y;
+        w[4 * u + 2] = q.z;
+        w[4 * u + 3] = q.w;
       }
       float acc = 0.0f;
+      uint32_t any = 0;
 #pragma unroll
-      for (int u = 0; u < kLoadsA; ++u) {
-        const uint32_t wv[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float2 f = decode2<DT>(wv[h]);
-          acc = __fmaf_rn(f.x, f.x, acc);
-          acc = __fmaf_rn(f.y, f.y, acc);
-          bad |= nonfinite2<DT>(wv[h]);
-        }
+      for (int h = 0; h < 4 * kLoadsA; ++h) {
+        const float2 f = decode2<DT>(w[h]);
+        acc = __fmaf_rn(f.x, f.x, acc);
+        acc = __fmaf_rn(f.y, f.y, acc);
+        any |= w[h];
+        bad |= nonfinite2<DT>(w[h]);
       }
-      total += double(acc);
+      total += partial_out_of_range<DT>(acc, any) ? trip_squares_fp64<DT, kLoadsA>(w)
+                                                  : double(acc);
     }
-    // The last (fewer than 8) elements of each staged sub-item: one thread each.
+    // The last (fewer than 8) elements of each staged sub-item: one thread
+    // each, squares in fp64.
     if (threadIdx.x < kStageA) {
       const int32_t len = s_len[threadIdx.x];
       const uint16_t* g = s_g[threadIdx.x];
-      float acc = 0.0f;
       for (int32_t e = len & ~7; e < len; ++e) {
         const uint16_t x = g[e];
-        const float f = decode1<DT>(x);
-        acc = __fmaf_rn(f, f, acc);
+        const double f = double(decode1<DT>(x));
+        total = fma(f, f, total);
         bad |= nonfinite2<DT>(uint32_t(x) | (uint32_t(x) << 16));
       }
-      total += double(acc);
     }
     // Staged pack items: a warp per small tensor.
     for (int jj = 0; jj < kStageA; ++jj) {
@@ -581,15 +630,24 @@ __global__ void exchange_trust_kernel(DevTables T) {
 }
 
 // ================================================ B: moments + norms pass
-template <int DT>
-__device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_t* __restrict__ g,
-                                              int64_t begin, int64_t n, int tid, int nthr,
-                                              const Elem& e, float& sw, float& sr) {
-  float* __restrict__ m = d.m + begin;
-  float* __restrict__ v = d.v + begin;
-  const float* __restrict__ w = d.w + begin;
+// Moments, direction and norms for elements [begin, begin + n) of one tensor:
+// m and v are read from (mi, vi) and the new ones written to (mo, vo) (the
+// same arrays except in speculative mode); thread tid of nthr takes 8-element
+// vectors tid, tid + nthr, ...  With G2 it also sums the raw g^2 and the
+// inf/NaN flag of the grads it reads (speculative mode's grad norm).
+template <int DT, bool G2>
+__device__ __forceinline__ void moments_range_io(const float* mi, const float* vi, float* mo,
+                                                 float* vo, const float* __restrict__ w, float wd,
+                                                 const uint16_t* __restrict__ g, int64_t begin,
+                                                 int64_t n, int tid, int nthr, const Elem& e,
+                                                 float& sw, float& sr, float& sg, double& sgd,
+                                                 uint32_t& bad) {
+  mi += begin;
+  vi += begin;
+  mo += begin;
+  vo += begin;
+  w += begin;
   g += begin;
-  const float wd = d.wd;
   const int64_t nv = n >> 3;
   constexpr int kUnroll = LAMB_UNROLL_B;
   for (int64_t k0 = tid; k0 < nv; k0 += int64_t(kUnroll) * nthr) {
@@ -602,8 +660,8 @@ __device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_
         gq[u] = ld_u4(g + 8 * k);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          put4(mr[u], h, ld_f4(m + 8 * k + 4 * h));
-          put4(vr[u], h, ld_f4(v + 8 * k + 4 * h));
+          put4(mr[u], h, ld_f4(mi + 8 * k + 4 * h));
+          put4(vr[u], h, ld_f4(vi + 8 * k + 4 * h));
           put4(wr[u], h, ld_f4(w + 8 * k + 4 * h));
         }
       }
@@ -613,11 +671,23 @@ __device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_
       const int64_t k = k0 + int64_t(u) * nthr;
       if (k < nv) {
         const uint32_t wv[4] = {gq[u].x, gq[u].y, gq[u].z, gq[u].w};
+        float pv = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 f = decode2<DT>(wv[j]);
+          if (G2) {
+            pv = __fmaf_rn(f.x, f.x, pv);
+            pv = __fmaf_rn(f.y, f.y, pv);
+            bad |= nonfinite2<DT>(wv[j]);
+          }
           e.moments(f.x, mr[u][2 * j], vr[u][2 * j]);
           e.moments(f.y, mr[u][2 * j + 1], vr[u][2 * j + 1]);
+        }
+        if (G2) {  // this vector's squares: fp32, or fp64 when out of range
+          if (partial_out_of_range<DT>(pv, wv[0] | wv[1] | wv[2] | wv[3]))
+            sgd += squares8_fp64<DT>(wv[0], wv[1], wv[2], wv[3]);
+          else
+            sg = __fadd_rn(sg, pv);
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -627,22 +697,40 @@ __device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          st_f4(m + 8 * k + 4 * h, get4(mr[u], h));
-          st_f4(v + 8 * k + 4 * h, get4(vr[u], h));
+          st_f4(mo + 8 * k + 4 * h, get4(mr[u], h));
+          st_f4(vo + 8 * k + 4 * h, get4(vr[u], h));
         }
       }
     }
   }
   for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {
-    float mj = m[j], vj = v[j];
+    float mj = mi[j], vj = vi[j];
     const float wj = w[j];
-    e.moments(decode1<DT>(g[j]), mj, vj);
+    const uint16_t x = g[j];
+    const float f = decode1<DT>(x);
+    if (G2) {  // fewer than 8: fp64 squares
+      sgd = fma(double(f), double(f), sgd);
+      bad |= nonfinite2<DT>(uint32_t(x) | (uint32_t(x) << 16));
+    }
+    e.moments(f, mj, vj);
     const float r = e.direction(mj, vj, wj, wd);
     sw = __fmaf_rn(wj, wj, sw);
     sr = __fmaf_rn(r, r, sr);
-    m[j] = mj;
-    v[j] = vj;
+    mo[j] = mj;
+    vo[j] = vj;
   }
+}
+
+// The same, in place on the tensor's m and v.
+template <int DT>
+__device__ __forceinline__ void moments_range(const TensorDesc& d, const uint16_t* __restrict__ g,
+                                              int64_t begin, int64_t n, int tid, int nthr,
+                                              const Elem& e, float& sw, float& sr) {
+  float sg = 0.0f;
+  double sgd = 0.0;
+  uint32_t bad = 0;
+  moments_range_io<DT, false>(d.m, d.v, d.m, d.v, d.w, d.wd, g, begin, n, tid, nthr, e, sw, sr,
+                              sg, sgd, bad);
 }
 
 // Apply for elements [begin, begin + n) of one tensor (kernel C, and packed
@@ -713,30 +801,118 @@ __device__ __forceinline__ void prefetch_item(const DevTables& T, int32_t it) {
   prefetch_l2(d.w + wi.begin, n * 4u);
 }
 
-template <int DT>
+// Waits (thread 0, bounded) until tensor i's trust ratio of this step is
+// published, then lets the whole CTA go on; false if the wait gave up.
+constexpr uint32_t kReadyPolls = 1u << 22;
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool wait_ready(const uint32_t* flag, uint32_t tag, int* shared_ok) {
+  if (threadIdx.x == 0) {
+    uint32_t polls = 0;
+    bool ok = true;
+    while (ld_acquire(flag) != tag) {
+      if (++polls > kReadyPolls) {
+        ok = false;
+        break;
+      }
+      __nanosleep(100);
+    }
+    *shared_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *shared_ok != 0;
+}
+
+// B (and, when FUSED, C too).  Items [0, n_items) of the work table are
+// moments items; with FUSED, virtual items [n_items, 2 n_items) are the apply
+// items of the same table, taken from the same counter after every moments
+// item has been handed out.  An apply item waits (bounded) until its tensor's
+// trust ratio is published by the CTA that finished the tensor's last
+// moments item; that CTA is running and never waits, so the wait ends.  CTAs
+// that run out of moments items so start applying finished tensors while the
+// last moments items drain, instead of idling until a second kernel starts.
+//
+// REDO (speculative mode only; launched after the speculative kernel, with
+// FUSED): runs only when that step turned out clipped (not skipped).  It
+// then reads m and v from the buffer set the step started from, which the
+// speculative pass left untouched, and writes the clipped moments over the
+// other set, which then holds the state; it uses the apply counters.
+template <int DT, bool FUSED, bool REDO>
 __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(DevTables T, Hyper hp) {
   __shared__ double2 red[kWarps];
   __shared__ int is_last;
   __shared__ int32_t slot;
+  __shared__ int ready_ok;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t n_virtual = FUSED ? 2 * T.n_items : T.n_items;
   // Before the wait: take the first item (this step's counter was reset one
   // step ago) and prefetch its first bytes; nothing the grad-norm kernel
   // writes is read here.
-  ItemQueue q{&T.queue[hp.parity], T.n_items, &slot, int32_t(blockIdx.x)};
+  ItemQueue q{&T.queue[REDO ? 2 + hp.parity : hp.parity], n_virtual, &slot, int32_t(blockIdx.x)};
   int32_t it = q.next();
-  if (threadIdx.x == 0 && it < T.n_items) prefetch_item<DT>(T, it);
+  if (!REDO && threadIdx.x == 0 && it < T.n_items) prefetch_item<DT>(T, it);
   pdl_wait();
   pdl_trigger();  // the apply kernel may launch as this grid drains
   const StepScalars* sc = T.sc;
   if (sc->skip) return;
+  if (REDO && sc->spec_ok) return;
+  const int32_t src = REDO ? sc->src : 0;  // REDO: read set src, write the other
   const Elem e{hp.b1, hp.b2, hp.omb1, hp.omb2, sc->c1, sc->c2, hp.eps, sc->gscale};
-  for (; it < T.n_items; it = q.next()) {
+  // This tensor's m, v to read and to write, and a descriptor whose m, v are
+  // the written ones (for the update).
+  auto io = [&](const TensorDesc& d, const float*& mi, const float*& vi, TensorDesc& dout) {
+    dout = d;
+    mi = d.m;
+    vi = d.v;
+    if (REDO) {
+      mi = src ? d.m2 : d.m;
+      vi = src ? d.v2 : d.v;
+      dout.m = src ? d.m : d.m2;
+      dout.v = src ? d.v : d.v2;
+    }
+  };
+  for (; it < n_virtual; it = q.next()) {
+    if (FUSED && it >= T.n_items) {
+      // ---- an apply item of a tensor with several items
+      const lamb_work_item wi = T.items[it - T.n_items];
+      if (wi.tensor < 0) continue;  // packs were finished in their moments item
+      const TensorDesc d0 = T.td[wi.tensor];
+      if (d0.n_items == 1) continue;  // so were tensors of one item
+      if (!wait_ready(&T.ready[wi.tensor], hp.tag, &ready_ok)) {
+        if (threadIdx.x == 0) {
+          atomicOr(reinterpret_cast<unsigned int*>(&T.sc->error), 1u);
+          if (hp.slot) static_cast<volatile ResultRecord*>(hp.slot)->error = 1;
+        }
+        continue;
+      }
+      const float* mi;
+      const float* vi;
+      TensorDesc d;
+      io(d0, mi, vi, d);
+      const float step = __fmul_rn(hp.lr, __ldcg(&T.trust[wi.tensor]));
+      apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
+      continue;
+    }
     const lamb_work_item wi = T.items[it];
     if (wi.tensor >= 0) {
-      const TensorDesc d = T.td[wi.tensor];
-      float sw = 0.0f, sr = 0.0f;
-      moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[wi.tensor]), wi.begin, wi.count,
-                        threadIdx.x, kThreads, e, sw, sr);
+      const float* mi;
+      const float* vi;
+      TensorDesc d;
+      io(T.td[wi.tensor], mi, vi, d);
+      float sw = 0.0f, sr = 0.0f, sg = 0.0f;
+      double sgd = 0.0;
+      uint32_t bad = 0;
+      moments_range_io<DT, false>(mi, vi, d.m, d.v, d.w, d.wd,
+                                  static_cast<const uint16_t*>(T.grads[wi.tensor]), wi.begin,
+                                  wi.count, threadIdx.x, kThreads, e, sw, sr, sg, sgd, bad);
       const double2 s = block_sum2(sw, sr, red);
       if (d.n_items == 1) {
         if (d.xslot >= 0) {  // shared with other ranks: out for summing
@@ -749,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
         // A tensor of one item is finished here, in one pass: every thread
         // re-reads only the elements it has just written or read itself (the
         // same thread-to-element map in both loops), so the update reads
-        // cache, not HBM, and the apply kernel skips the item.
+        // cache, not HBM, and the apply pass skips the item.
         const float tr = trust_of(s.x, s.y);
         if (threadIdx.x == 0) T.trust[wi.tensor] = tr;
         apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, __fmul_rn(hp.lr, tr));
@@ -779,6 +955,10 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
             T.xt[2 * d.xslot + 1] = tot.y;
           } else {
             T.trust[wi.tensor] = trust_of(tot.x, tot.y);
+            if (FUSED) {  // publish: the tensor's apply items may start
+              __threadfence();
+              st_release(&T.ready[wi.tensor], hp.tag);
+            }
           }
           T.tensor_ticket[wi.tensor] = 0u;
         }
@@ -788,15 +968,216 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
       // moments and norms, trust, then the update.  Each lane re-reads only
       // the elements it has just written or read itself (same lane-to-element
       // map in both passes), so the second pass hits cache, not HBM, and needs
-      // no synchronisation; the apply kernel skips pack items.
+      // no synchronisation; the apply pass skips pack items.
       for (int k = warp; k < wi.count; k += kWarps) {
         const int32_t ti = T.pack_ids[wi.begin + k];
-        const TensorDesc d = T.td[ti];
-        float sw = 0.0f, sr = 0.0f;
-        moments_range<DT>(d, static_cast<const uint16_t*>(T.grads[ti]), 0, d.n, lane, 32, e, sw,
-                          sr);
+        const float* mi;
+        const float* vi;
+        TensorDesc d;
+        io(T.td[ti], mi, vi, d);
+        float sw = 0.0f, sr = 0.0f, sg = 0.0f;
+        double sgd = 0.0;
+        uint32_t bad = 0;
+        moments_range_io<DT, false>(mi, vi, d.m, d.v, d.w, d.wd,
+                                    static_cast<const uint16_t*>(T.grads[ti]), 0, d.n, lane, 32,
+                                    e, sw, sr, sg, sgd, bad);
         const double a = warp_sum(double(sw)), b = warp_sum(double(sr));
         const float tr = trust_of(a, b);
+        if (lane == 0) T.trust[ti] = tr;
+        apply_range(d, 0, d.n, lane, 32, e, __fmul_rn(hp.lr, tr));
+      }
+    }
+  }
+#ifdef LAMB_TEST_APPLY_REPORTS_WAIT_ERROR
+  // Test builds only: CTA 0 reports a given-up wait after finishing its work
+  // normally (no wait actually runs out), so that the host's handling of the
+  // error can be tested.
+  if (FUSED && !REDO) {
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      atomicOr(reinterpret_cast<unsigned int*>(&T.sc->error), 1u);
+      if (hp.slot) static_cast<volatile ResultRecord*>(hp.slot)->error = 1;
+    }
+  }
+#endif
+}
+
+// ============================ speculative mode: the grad-norm pass folded in
+// One persistent grid per step, for a handle with a second set of m and v
+// buffers.  Items [0, n_items) are moments items: each reads g, m, v and w
+// once, sums the raw g^2 and the inf/NaN flag on the way (what the grad-norm
+// kernel reads g for), and writes m' and v' -- computed as if the step were
+// neither skipped nor clipped -- to the set the step did not start from, so
+// the state stays untouched until the step is known to stand.  The CTA that
+// finishes the last moments item adds the per-item g^2 partials in item
+// order, publishes the step (publish_step) and releases a flag; the apply
+// items [n_items, 2 n_items) wait (bounded) for the flag and, if the step
+// stands, apply the update from the written set, which then holds the state.
+// A clipped step is redone by the REDO moments kernel launched after this
+// one; a skipped step leaves the state where it was.  Apply items are handed
+// out only after every moments item, and moments items never wait, so every
+// wait ends.  Trust ratios, norms and moments use the same functions and the
+// same item-ordered sums as an ordinary step, so a step that stands matches
+// it bit for bit (the grad norm is summed in a different order).
+template <int DT>
+__global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) spec_step_kernel(DevTables T, Hyper hp,
+                                                                               NormArgs na,
+                                                                               ScaleArgs sa) {
+  __shared__ double2 red[kWarps];
+  __shared__ double red1[kWarps];
+  __shared__ double warp_g2[kWarps];
+  __shared__ int is_last;
+  __shared__ int is_final;
+  __shared__ int32_t slot;
+  __shared__ int ready_ok;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t n = T.n_items;
+  StepScalars* sc = T.sc;
+  ItemQueue q{&T.queue[hp.parity], 2 * n, &slot, int32_t(blockIdx.x)};
+  bool have_state = false, have_apply = false, stands = false;
+  Elem e{};
+  int32_t src = 0;
+  for (int32_t it = q.next(); it < 2 * n; it = q.next()) {
+    if (it < n) {
+      if (!have_state) {
+        // The scalars that do not depend on the grad norm, read only after
+        // taking a moments item: the step's publisher (which needs this
+        // item finished first) advances them for the next step.
+        const bool host_t = na.t_host > 0;
+        const double p1 = host_t ? na.p1_host : sc->p1_next;
+        const double p2 = host_t ? na.p2_host : sc->p2_next;
+        const float S = sa.dynamic ? sc->scale : sa.fixed;
+        e = Elem{hp.b1, hp.b2, hp.omb1, hp.omb2, float(1.0 / (1.0 - p1)),
+                 float(1.0 / (1.0 - p2)), hp.eps, float(1.0 / double(S))};
+        src = sc->cur;
+        have_state = true;
+      }
+      const lamb_work_item wi = T.items[it];
+      uint32_t bad = 0;
+      double item_g2 = 0.0;
+      if (wi.tensor >= 0) {
+        const TensorDesc d = T.td[wi.tensor];
+        float sw = 0.0f, sr = 0.0f, sg = 0.0f;
+        double sgd = 0.0;
+        moments_range_io<DT, true>(src ? d.m2 : d.m, src ? d.v2 : d.v, src ? d.m : d.m2,
+                                   src ? d.v : d.v2, d.w, d.wd,
+                                   static_cast<const uint16_t*>(T.grads[wi.tensor]), wi.begin,
+                                   wi.count, threadIdx.x, kThreads, e, sw, sr, sg, sgd, bad);
+        const double2 s = block_sum2(sw, sr, red);
+        item_g2 = block_sum(double(sg) + sgd, red1);
+        if (d.n_items == 1) {
+          if (threadIdx.x == 0) T.trust_spec[wi.tensor] = trust_of(s.x, s.y);
+        } else {
+          if (threadIdx.x == 0) {
+            T.item_wr[it] = s;
+            __threadfence();
+            const uint32_t prev = atomicAdd(&T.tensor_ticket[wi.tensor], 1u);
+            is_last = prev == uint32_t(d.n_items - 1);
+          }
+          __syncthreads();
+          if (is_last) {
+            __threadfence();
+            double a = 0.0, b = 0.0;
+            for (int32_t k = threadIdx.x; k < d.n_items; k += kThreads) {
+              const double2 x = __ldcg(&T.item_wr[d.first_item + k]);
+              a += x.x;
+              b += x.y;
+            }
+            const double2 tot = block_sum2(a, b, red);
+            if (threadIdx.x == 0) {
+              T.trust_spec[wi.tensor] = trust_of(tot.x, tot.y);
+              T.tensor_ticket[wi.tensor] = 0u;
+            }
+          }
+        }
+      } else {
+        // A pack: a warp per small tensor (moments, norms, trust; the update
+        // waits for the apply items).  The pack's g^2 is summed per warp in
+        // the warp's tensor order, then over the warps in warp order.
+        double wg = 0.0;
+        for (int k = warp; k < wi.count; k += kWarps) {
+          const int32_t ti = T.pack_ids[wi.begin + k];
+          const TensorDesc d = T.td[ti];
+          float sw = 0.0f, sr = 0.0f, sg = 0.0f;
+          double sgd = 0.0;
+          moments_range_io<DT, true>(src ? d.m2 : d.m, src ? d.v2 : d.v, src ? d.m : d.m2,
+                                     src ? d.v : d.v2, d.w, d.wd,
+                                     static_cast<const uint16_t*>(T.grads[ti]), 0, d.n, lane, 32,
+                                     e, sw, sr, sg, sgd, bad);
+          const double a = warp_sum(double(sw)), b = warp_sum(double(sr));
+          wg += warp_sum(double(sg) + sgd);
+          if (lane == 0) T.trust_spec[ti] = trust_of(a, b);
+        }
+        if (lane == 0) warp_g2[warp] = wg;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          double t = 0.0;
+          for (int k = 0; k < kWarps; ++k) t += warp_g2[k];
+          item_g2 = t;
+        }
+      }
+      bad = __syncthreads_or(bad);
+      // One more moments item done; the CTA that finishes the last one
+      // publishes the step.
+      if (threadIdx.x == 0) {
+        T.item_g2[it] = item_g2;
+        if (bad) atomicOr(&sc->nonfinite, 1u);
+        __threadfence();
+        const uint32_t prev = atomicAdd(&sc->items_done, 1u);
+        is_final = prev == uint32_t(n - 1);
+      }
+      __syncthreads();
+      if (is_final) {
+        __threadfence();
+        double g2 = 0.0;
+        for (int32_t k = threadIdx.x; k < n; k += kThreads) g2 += __ldcg(&T.item_g2[k]);
+        g2 = block_sum(g2, red1);
+        if (threadIdx.x == 0) {
+          const uint32_t nf = atomicExch(&sc->nonfinite, 0u);
+          sc->items_done = 0u;
+          const int32_t cur = sc->cur;
+          const bool clipped = publish_step(T, na, sa, g2, nf != 0u);
+          sc->src = cur;
+          sc->spec_ok = (!nf && !clipped) ? 1 : 0;
+          sc->cur = nf ? cur : 1 - cur;
+          if (na.slot) static_cast<volatile ResultRecord*>(na.slot)->state_buf = sc->cur;
+          __threadfence();
+          st_release(&sc->published, hp.tag);
+        }
+      }
+      continue;
+    }
+    // ---- an apply item: wait until the step is published
+    if (!have_apply) {
+      if (!wait_ready(&sc->published, hp.tag, &ready_ok)) {
+        if (threadIdx.x == 0) {
+          atomicOr(reinterpret_cast<unsigned int*>(&sc->error), 1u);
+          if (hp.slot) static_cast<volatile ResultRecord*>(hp.slot)->error = 1;
+        }
+        break;
+      }
+      stands = __ldcg(&sc->spec_ok) != 0;
+      src = __ldcg(&sc->src);
+      e = Elem{hp.b1, hp.b2, hp.omb1, hp.omb2, __ldcg(&sc->c1), __ldcg(&sc->c2), hp.eps, 0.0f};
+      have_apply = true;
+    }
+    if (!stands) continue;  // skipped (nothing to do) or clipped (the redo kernel's job)
+    const lamb_work_item wi = T.items[it - n];
+    // The step stands: its trust ratios become the last step's (lamb_get_trust).
+    if (wi.tensor >= 0) {
+      TensorDesc d = T.td[wi.tensor];
+      d.m = src ? d.m : d.m2;  // the set this step wrote
+      d.v = src ? d.v : d.v2;
+      const float tr = __ldcg(&T.trust_spec[wi.tensor]);
+      if (threadIdx.x == 0 && wi.begin == 0) T.trust[wi.tensor] = tr;
+      apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, __fmul_rn(hp.lr, tr));
+    } else {
+      for (int k = warp; k < wi.count; k += kWarps) {
+        const int32_t ti = T.pack_ids[wi.begin + k];
+        TensorDesc d = T.td[ti];
+        d.m = src ? d.m : d.m2;
+        d.v = src ? d.v : d.v2;
+        const float tr = __ldcg(&T.trust_spec[ti]);
         if (lane == 0) T.trust[ti] = tr;
         apply_range(d, 0, d.n, lane, 32, e, __fmul_rn(hp.lr, tr));
       }
@@ -805,6 +1186,11 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
 }
 
 // ========================================================= C: apply pass
+// LAMB_TMA_C=1 (default): the TMA-staged apply kernel below; 0: this one.
+#ifndef LAMB_TMA_C
+#define LAMB_TMA_C 1
+#endif
+#if !LAMB_TMA_C
 __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTables T, Hyper hp) {
   __shared__ int32_t slot;
   ItemQueue q{&T.queue[2 + hp.parity], T.n_items, &slot, int32_t(blockIdx.x)};
@@ -822,6 +1208,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTa
     apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
   }
 }
+#endif
 
 // ====================== C, TMA-staged: m, v, w through shared memory (default)
 // Per item, pieces of kTmaPiece elements of m, v and w are bulk-copied
@@ -835,9 +1222,6 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTa
 // wait gives up (only if copies never arrive), the CTA records an error in
 // StepScalars, lets its copies in flight land (bounded) and leaves; the host
 // reports the step as failed.
-#ifndef LAMB_TMA_C
-#define LAMB_TMA_C 1
-#endif
 #if LAMB_TMA_C
 constexpr int kTmaPiece = kThreads * 8;  // 2048 elements: 8 per thread
 #ifndef LAMB_TMA_STAGES
@@ -995,10 +1379,25 @@ int max_blocks_per_sm(int kernel, int grad_dtype) {
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                      &nb, grad_norm_kernel<LAMB_GRAD_BF16>, kThreads, 0);
   } else if (kernel == 1) {
+    // The fused and the plain moments kernel share one launch shape: take
+    // the smaller of the two.
+    int nf = 0;
     err = fp16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                     &nb, moments_kernel<LAMB_GRAD_FP16>, kThreads, 0)
+                     &nb, moments_kernel<LAMB_GRAD_FP16, false, false>, kThreads, 0)
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                     &nb, moments_kernel<LAMB_GRAD_BF16>, kThreads, 0);
+                     &nb, moments_kernel<LAMB_GRAD_BF16, false, false>, kThreads, 0);
+    if (err == cudaSuccess)
+      err = fp16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &nf, moments_kernel<LAMB_GRAD_FP16, true, false>, kThreads, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &nf, moments_kernel<LAMB_GRAD_BF16, true, false>, kThreads, 0);
+    if (nf < nb) nb = nf;
+    if (err == cudaSuccess)
+      err = fp16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &nf, spec_step_kernel<LAMB_GRAD_FP16>, kThreads, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &nf, spec_step_kernel<LAMB_GRAD_BF16>, kThreads, 0);
+    if (nf < nb) nb = nf;
   } else {
 #if LAMB_TMA_C
     err = cudaFuncSetAttribute(apply_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1023,6 +1422,23 @@ int launch_grad_norm(const DevTables& T, int grid, int grad_dtype, const NormArg
     grad_norm_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, na, sa);
   else
     grad_norm_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, na, sa);
+  return int(cudaGetLastError());
+}
+
+int launch_spec_step(const DevTables& T, int grid, int grad_dtype, const Hyper& hp,
+                     const NormArgs& na, const ScaleArgs& sa, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (grad_dtype == LAMB_GRAD_FP16)
+    spec_step_kernel<LAMB_GRAD_FP16><<<grid, kThreads, 0, s>>>(T, hp, na, sa);
+  else
+    spec_step_kernel<LAMB_GRAD_BF16><<<grid, kThreads, 0, s>>>(T, hp, na, sa);
+  return int(cudaGetLastError());
+}
+
+__global__ void set_cur_kernel(StepScalars* sc, int32_t cur) { sc->cur = cur; }
+
+int launch_set_cur(StepScalars* sc, int32_t cur, void* stream) {
+  set_cur_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(sc, cur);
   return int(cudaGetLastError());
 }
 
@@ -1067,12 +1483,16 @@ struct DependentLaunch {
 };
 }  // namespace
 
-int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream) {
+int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, bool fused,
+                   void* stream) {
   DependentLaunch L(grid, 0, stream);
-  const cudaError_t e =
-      grad_dtype == LAMB_GRAD_FP16
-          ? cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_FP16>, T, hp)
-          : cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_BF16>, T, hp);
+  cudaError_t e;
+  if (grad_dtype == LAMB_GRAD_FP16)
+    e = fused ? cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_FP16, true, false>, T, hp)
+              : cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_FP16, false, false>, T, hp);
+  else
+    e = fused ? cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_BF16, true, false>, T, hp)
+              : cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_BF16, false, false>, T, hp);
   return e != cudaSuccess ? int(e) : int(cudaGetLastError());
 }
 
@@ -1084,6 +1504,15 @@ int launch_apply(const DevTables& T, int grid, const Hyper& hp, void* stream) {
   DependentLaunch L(grid, 0, stream);
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, apply_kernel, T, hp);
 #endif
+  return e != cudaSuccess ? int(e) : int(cudaGetLastError());
+}
+
+int launch_spec_redo(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, void* stream) {
+  DependentLaunch L(grid, 0, stream);
+  const cudaError_t e =
+      grad_dtype == LAMB_GRAD_FP16
+          ? cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_FP16, true, true>, T, hp)
+          : cudaLaunchKernelEx(&L.cfg, moments_kernel<LAMB_GRAD_BF16, true, true>, T, hp);
   return e != cudaSuccess ? int(e) : int(cudaGetLastError());
 }
 

@@ -221,11 +221,36 @@ class Lamb:
         check(self._lib.lamb_split_apply(self._h, ctypes.byref(seq)))
         return int(seq.value)
 
-    def one_pass_params(self) -> int:
-        """Elements whose whole step the moments kernel finishes (30 B/param)."""
-        n = ctypes.c_int64()
-        check(self._lib.lamb_one_pass_params(self._h, ctypes.byref(n)))
-        return int(n.value)
+    def info(self) -> dict:
+        """What the handle was built with: n_params, one_pass_params (elements
+        whose whole step the moments kernel finishes, at 30 B/param),
+        chunk_elems, n_items, and fused (moments and apply in one kernel)."""
+        out = _lib.LambInfo()
+        check(self._lib.lamb_get_info(self._h, ctypes.byref(out)))
+        return {k: int(getattr(out, k)) for k, _ in out._fields_}
+
+    def set_speculative(self, exp_avg2: Sequence[torch.Tensor] | None,
+                        exp_avg_sq2: Sequence[torch.Tensor] | None) -> None:
+        """Turn speculative mode on with a second set of m and v tensors (fp32,
+        the state's sizes, caller-owned), or off with ``None, None``."""
+        if exp_avg2 is None and exp_avg_sq2 is None:
+            check(self._lib.lamb_set_speculative(self._h, None, None))
+            self._second = None
+            return
+        _check_tensors("exp_avg2", exp_avg2, torch.float32, self.sizes, self.device)
+        _check_tensors("exp_avg_sq2", exp_avg_sq2, torch.float32, self.sizes, self.device)
+        second = (list(exp_avg2), list(exp_avg_sq2))
+        check(self._lib.lamb_set_speculative(self._h, _ptrs(second[0]), _ptrs(second[1])))
+        self._second = second
+
+    def state_buffers(self):
+        """The (m, v) tensor lists that hold the state now (speculative mode
+        alternates between the two sets; waits for the stream)."""
+        which = ctypes.c_int32()
+        check(self._lib.lamb_state_buffers(self._h, ctypes.byref(which)))
+        if which.value and getattr(self, "_second", None) is not None:
+            return self._second
+        return self._keep[1], self._keep[2]
 
     def set_step(self, t: int) -> None:
         """Set the GPU's step counter: the t of the next ``step_async``."""

@@ -116,13 +116,24 @@ def compare_state(st: W.State, hs: HostState, rtol: float, tag: str, opt: Lamb =
     return {"bf16_mismatch": mism, "checked": count}
 
 
+class CurrentState:
+    """A state whose m and v are the buffers that hold it now (speculative
+    mode alternates between two sets)."""
+
+    def __init__(self, st: W.State, opt: Lamb):
+        self.wl, self.w, self.w16 = st.wl, st.w, st.w16
+        self.m, self.v = opt.state_buffers()
+
+
 def run_parity(wl: W.Workload, steps: int, check_steps: Iterable[int] = (),
-               subset: Optional[Sequence[int]] = None, device: str = "cuda") -> dict:
+               subset: Optional[Sequence[int]] = None, device: str = "cuda",
+               speculative: bool = False) -> dict:
     """Runs ``steps`` steps of the GPU path and the oracle side by side.
 
     Every step compares the skip flag and the grad norm; the steps in
     ``check_steps`` also compare w, m, v, the bf16 copy and the trust ratios
-    of the tensors in ``subset`` (all tensors if None)."""
+    of the tensors in ``subset`` (all tensors if None).  ``speculative`` runs
+    the library in speculative mode, with a second set of m and v buffers."""
     check_steps = set(check_steps)
     st = W.make_state(wl, device)
     hs = HostState(st, subset)
@@ -130,6 +141,10 @@ def run_parity(wl: W.Workload, steps: int, check_steps: Iterable[int] = (),
     opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, beta1=wl.beta1, beta2=wl.beta2,
                eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype)
     opt.set_grads(gviews)
+    if speculative:
+        m2, v2 = torch.empty_like(st.m_flat), torch.empty_like(st.v_flat)
+        opt.set_speculative(st.views(m2), st.views(v2))
+        assert opt.info()["speculative"] == 1
     t = wl.t0
     log = {"skipped": [], "bf16_mismatch": 0, "checked": 0}
     try:
@@ -147,7 +162,8 @@ def run_parity(wl: W.Workload, steps: int, check_steps: Iterable[int] = (),
                 assert_close(np.array([gn]), np.array([ogn]), rtol_for(k), f"step {k} grad_norm")
                 t += 1
             if k in check_steps:
-                r = compare_state(st, hs, rtol_for(k), f"step {k}", opt,
+                cur = CurrentState(st, opt) if speculative else st
+                r = compare_state(cur, hs, rtol_for(k), f"step {k}", opt,
                                   None if osk else otrust)
                 log["bf16_mismatch"] += r["bf16_mismatch"]
                 log["checked"] += r["checked"]

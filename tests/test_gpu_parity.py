@@ -224,6 +224,11 @@ def test_bf16_copies_land_in_one_allgather_bucket():
     dict(beta1=0.5, beta2=0.75, eps=0.5),  # large eps dominates sqrt(v)
     dict(sigma=3.0e4),                     # bf16 grads near 1e5 (large squares)
     dict(sigma=1e-15),                     # tiny grads: squares near 1e-30
+    # bf16 grads whose squares leave fp32's normal range: below 2^-126
+    # (summed in fp64 instead of fp32) and, with clipping, so large that 128
+    # of their squares would overflow fp32
+    dict(sigma=1e-21),
+    dict(sigma=3e19),
 ])
 def test_hyperparameter_corner_cases(case):
     case = dict(case)

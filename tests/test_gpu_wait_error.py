@@ -1,11 +1,13 @@
-"""The host's handling of a bounded wait that gives up inside the apply
-kernel (staged copies from HBM that never arrive).
+"""The host's handling of a bounded wait that gives up inside the step's
+apply pass (TMA copies from HBM that never arrive, or a tensor's trust ratio
+that is never published to the fused moments-and-apply kernel).
 
 No wait is ever made to run out here.  A test build of the library
-(LAMB_TEST_APPLY_REPORTS_WAIT_ERROR) has CTA 0 of the apply kernel report a
-given-up wait after it has finished its work normally, with no copy in
-flight; the test checks that lamb_step and lamb_step_result then return
-LAMB_ERR_CUDA with the message that the state of the step is undefined.
+(LAMB_TEST_APPLY_REPORTS_WAIT_ERROR) has CTA 0 of the kernel that applies the
+update report a given-up wait after it has finished its work normally, with
+nothing in flight; the test checks that lamb_step and lamb_step_result then
+return LAMB_ERR_CUDA with the message that the state of the step is
+undefined.
 """
 import ctypes
 
