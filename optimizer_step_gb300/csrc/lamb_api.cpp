@@ -168,6 +168,20 @@ bool check_step_args(lamb_handle* h, const void* const* grads, float lr, float c
 // Enqueues one step (arguments already checked) on the handle's stream: the
 // grad pointers if new, the three kernels, and the event of its result slot.
 // t_host >= 1 fixes the step number; 0 takes it from the device counter.
+// Clears the result-ring slot of step seq before the step is enqueued.  If
+// the step that used the slot last (seq - 64) has not finished on the GPU,
+// waits for it first.
+int claim_slot(lamb_handle* h, int64_t seq) {
+  const int r = int(seq % kResultRing);
+  if (seq >= kResultRing) {
+    const cudaError_t ce = cudaEventSynchronize(h->ring_ev[r]);
+    if (ce != cudaSuccess) return cuda_fail(ce, "waiting for a result slot");
+  }
+  std::memset(h->ring + r, 0, sizeof(ResultRecord));
+  std::atomic_thread_fence(std::memory_order_release);
+  return LAMB_OK;
+}
+
 int select_grads(lamb_handle* h, const void* const* grads) {
   // Find this step's grad pointers among the device slots, or write them
   // into the next slot.  The write is a kernel on the handle's stream, so it
@@ -242,6 +256,7 @@ int enqueue_step(lamb_handle* h, const void* const* grads, float lr, int64_t t_h
   if (rc) return rc;
   const int64_t seq = h->next_seq;
   const int r = int(seq % kResultRing);
+  if ((rc = claim_slot(h, seq)) != LAMB_OK) return rc;
   const Hyper hy = make_hyper(h, lr, seq);
   const NormArgs na = make_norm_args(h, clip, t_host, seq, 0);
   if ((ce = mark(h, r, 0)) != cudaSuccess) return cuda_fail(ce, "event record");
@@ -394,7 +409,18 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
   if (!h) return fail(LAMB_ERR_NOMEM, "host allocation failed");
   std::string err;
   const int64_t chunk = choose_chunk(n_params, int64_t(sms) * per_sm[1]);
-  if (!build_plan(n_tensors, sizes, chunk, no_pack.data(), &h->plan, &err)) {
+  if (!build_plan(n_tensors, sizes, chunk, no_pack.data(), 0, &h->plan, &err)) {
+    delete h;
+    return fail(LAMB_ERR_INVALID, err);
+  }
+  // A shard of few waves runs the fused kernel; its last tensor then gets
+  // half-size chunks (measured on GB300: 132.3 -> 130.5 us at 16.8 M params,
+  // a tie at 4.2 M and 67 M; on a 1.8 B-param shard, which runs three
+  // kernels, the same split cost 0.85%).
+  const bool fused = !h->plan.items.empty() &&
+                     int64_t(h->plan.items.size()) <=
+                         int64_t(LAMB_FUSED_MAX_WAVES) * int64_t(per_sm[1]) * sms;
+  if (fused && !build_plan(n_tensors, sizes, chunk, no_pack.data(), 1, &h->plan, &err)) {
     delete h;
     return fail(LAMB_ERR_INVALID, err);
   }
@@ -512,7 +538,7 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
     const int64_t full = int64_t(per_sm[k]) * sms;
     h->grid[k] = int(std::max<int64_t>(1, std::min<int64_t>(full, int64_t(ni))));
   }
-  h->fused = int64_t(ni) <= int64_t(LAMB_FUSED_MAX_WAVES) * h->grid[1] && ni > 0;
+  h->fused = fused;
   // Sub-items per chunk item for the grad-norm kernel: about kSplitTarget per
   // CTA of its full grid, sub-items of at least kMinSubItem elements.
   {
@@ -631,9 +657,11 @@ LAMB_API int lamb_split_moments(lamb_handle* h, float lr, int64_t t, float clip)
   if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
   const int64_t seq = h->next_seq;
   const int r = int(seq % kResultRing);
+  int rc = claim_slot(h, seq);
+  if (rc != LAMB_OK) return rc;
   ScaleArgs sa = h->scaler;
   sa.fixed = h->split_scale;
-  int rc = launch_finalize(h->T, make_norm_args(h, clip, t, seq, 0), sa, h->stream);
+  rc = launch_finalize(h->T, make_norm_args(h, clip, t, seq, 0), sa, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "finalize kernel launch");
   if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
   cudaError_t ce = mark(h, r, 1);

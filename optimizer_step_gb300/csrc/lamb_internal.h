@@ -45,9 +45,10 @@ struct Plan {
 
 // Builds the work table; returns false (with a message) on invalid sizes or
 // a table too large for 32-bit item indices.  Tensors with no_pack[i] != 0
-// (no_pack may be NULL) get chunk items even when small.
+// (no_pack may be NULL) get chunk items even when small.  tail_shift > 0
+// cuts the last tensor of several chunks into chunks 2^tail_shift smaller.
 bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
-                const uint8_t* no_pack, Plan* plan, std::string* err);
+                const uint8_t* no_pack, int tail_shift, Plan* plan, std::string* err);
 
 // Per-tensor record the kernels read (device copy built at create time).
 struct TensorDesc {
@@ -76,6 +77,8 @@ struct StepScalars {
   float scale;         // dynamic loss scale for the next step
   int32_t good_steps;  // clean steps in a row since the last growth/backoff
   int32_t error;       // set on the GPU if a bounded wait gave up this step
+  float scale_next;    // S the next step uses (scale, or scale_used when it is fixed)
+  int32_t pad0;
   float c1, c2;        // 1/(1-beta1^t), 1/(1-beta2^t) of this step
   int64_t t_used;      // the step number t of this step
   int64_t t_next;      // the step number of the next step (advances on clean steps)

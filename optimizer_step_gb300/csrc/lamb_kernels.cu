@@ -383,6 +383,20 @@ __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int6
   }
 }
 
+// The host's copy of a step's outcome, written by the step's publisher into
+// its slot of the pinned, device-mapped result ring (the host cleared the
+// slot when it enqueued the step; a bounded wait that gives up sets its
+// error field).  Writing it one kernel later instead, off the publishing
+// CTA's path, measured the same on GB300.
+__device__ __forceinline__ void write_record(const StepScalars* sc, ResultRecord* slot) {
+  volatile ResultRecord* r = slot;
+  r->grad_norm = sc->grad_norm;
+  r->t_used = sc->t_used;
+  r->scale_used = sc->scale_used;
+  r->scale_next = sc->scale_next;
+  r->skipped = sc->skip;
+}
+
 // Publishes one step's scalars from the sum of raw g^2 over the shard (or the
 // data-parallel group) and the inf/NaN flag: the grad norm ||g/S||, the clip
 // factor, the skip flag, the step number t and its bias corrections (from
@@ -434,15 +448,8 @@ __device__ bool publish_step(const DevTables& T, const NormArgs& na, const Scale
     }
     sc->scale = next;
   }
-  if (na.slot) {  // the host's copy of the outcome, in mapped pinned memory
-    volatile ResultRecord* r = na.slot;
-    r->grad_norm = sc->grad_norm;
-    r->t_used = t;
-    r->scale_used = S;
-    r->scale_next = sa.dynamic ? sc->scale : S;
-    r->skipped = nf ? 1 : 0;
-    r->error = 0;
-  }
+  sc->scale_next = sa.dynamic ? sc->scale : S;
+  if (na.slot) write_record(sc, na.slot);
   sc->error = 0;  // no wait of this step has given up yet
   // Item counters of the next step's moments and apply kernels (the other
   // parity; this step's were reset one step ago, so this step's kernels can
@@ -1140,9 +1147,9 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) spec_step_kernel(D
           sc->src = cur;
           sc->spec_ok = (!nf && !clipped) ? 1 : 0;
           sc->cur = nf ? cur : 1 - cur;
-          if (na.slot) static_cast<volatile ResultRecord*>(na.slot)->state_buf = sc->cur;
           __threadfence();
           st_release(&sc->published, hp.tag);
+          if (na.slot) static_cast<volatile ResultRecord*>(na.slot)->state_buf = sc->cur;
         }
       }
       continue;

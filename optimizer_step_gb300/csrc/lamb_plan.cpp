@@ -21,20 +21,17 @@ namespace lambgb {
 // shards then give each CTA one or two large items instead of several small
 // ones, which matters because each item costs a chain of dependent latencies
 // (table, data, block reduction, ticket); large shards get full-size chunks.
-#ifndef LAMB_MIN_WAVES
-#define LAMB_MIN_WAVES 1
-#endif
 int64_t choose_chunk(int64_t n_params, int64_t cta_slots) {
   const int64_t slots = std::max<int64_t>(1, cta_slots);
-  const int64_t waves = std::max<int64_t>(LAMB_MIN_WAVES, (n_params + slots * kChunkElems - 1) /
-                                                              (slots * kChunkElems));
+  const int64_t waves = std::max<int64_t>(1, (n_params + slots * kChunkElems - 1) /
+                                                 (slots * kChunkElems));
   int64_t c = (n_params + waves * slots - 1) / (waves * slots);
   c = (c + 255) / 256 * 256;
   return std::min(kChunkElems, std::max(kMinChunkElems, c));
 }
 
 bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
-                const uint8_t* no_pack, Plan* plan, std::string* err) {
+                const uint8_t* no_pack, int tail_shift, Plan* plan, std::string* err) {
   plan->items.clear();
   plan->pack_ids.clear();
   plan->first_item.assign(size_t(std::max(n_tensors, 0)), -1);
@@ -80,10 +77,10 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
   // not be packed), each tensor's chunks contiguous: first the tensors of a
   // single chunk (the moments kernel finishes them in one pass, a chain of
   // latencies that should not trail at the end of the kernel), then the rest.
-#ifndef LAMB_TAIL_SPLIT
-#define LAMB_TAIL_SPLIT 0
-#endif
-  int32_t last_multi = -1;  // the last tensor of several chunks: its chunks end the table
+  // The last tensor of several chunks ends the table; with tail_shift its
+  // chunks are 2^tail_shift times smaller, so that the last items of a
+  // kernel that has only a few waves of them finish closer together.
+  int32_t last_multi = -1;
   for (int32_t i = 0; i < n_tensors; ++i)
     if (sizes[i] > chunk_elems) last_multi = i;
   for (int pass = 0; pass < 2; ++pass)
@@ -91,7 +88,7 @@ bool build_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_elems,
     const int64_t n = sizes[i];
     if (n == 0 || (n <= kSmallMax && !(no_pack && no_pack[i]))) continue;
     if ((n <= chunk_elems) != (pass == 0)) continue;
-    const int64_t c = i == last_multi ? std::max<int64_t>(kMinChunkElems, chunk_elems >> LAMB_TAIL_SPLIT)
+    const int64_t c = i == last_multi ? std::max<int64_t>(kMinChunkElems, chunk_elems >> tail_shift)
                                       : chunk_elems;
     const int64_t nchunks = (n + c - 1) / c;
     int64_t per = (n + nchunks - 1) / nchunks;
@@ -125,7 +122,7 @@ LAMB_API int lamb_plan(int32_t n_tensors, const int64_t* sizes, int64_t chunk_el
   lambgb::Plan plan;
   std::string err;
   if (chunk_elems == 0) chunk_elems = lambgb::kChunkElems;
-  if (!lambgb::build_plan(n_tensors, sizes, chunk_elems, nullptr, &plan, &err)) {
+  if (!lambgb::build_plan(n_tensors, sizes, chunk_elems, nullptr, 0, &plan, &err)) {
     lambgb::set_last_error(err);
     return LAMB_ERR_INVALID;
   }
