@@ -240,11 +240,14 @@ LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq);
  *               dynamic loss scaler is on)
  *   out         receives {skipped, grad_norm, loss_scale, next_loss_scale}
  *
- * Enqueues three kernels on the handle's stream (grad norm, moments and
- * per-tensor norms, apply), then copies the small outcome record to pinned
- * host memory and waits for it: the call returns when the step has finished
- * on the GPU.  The skip decision is taken on the GPU; the host never reads it in
- * the middle of a step.  Each step's grad-pointer set is matched against four
+ * Enqueues the step's kernels on the handle's stream -- the grad-norm
+ * kernel, then one persistent moments-and-apply kernel when the work table
+ * holds at most 8 waves of items (lamb_get_info's fused), else the moments
+ * and per-tensor norms kernel and the apply kernel; in speculative mode
+ * (lamb_set_speculative) one kernel and the redo kernel -- and waits for the
+ * outcome record, which the GPU writes into pinned host memory: the call
+ * returns when the step has finished on the GPU.  The skip decision is taken
+ * on the GPU; the host never reads it in the middle of a step.  Each step's grad-pointer set is matched against four
  * device slots, so alternating among up to four grad buffers costs no upload;
  * a new set is written by a small kernel, never by a copy (a copy could queue
  * behind unrelated bulk transfers on the copy engine).
@@ -423,15 +426,19 @@ LAMB_API int lamb_get_trust(lamb_handle* h, float* host_out, int32_t n_tensors);
  * CUDA event monitor (after the per-rank CUDA-event timing of MegaScale's
  * guided-reading digest, section 7: critical segments are timed with CUDA
  * events instead of host timers, so timing forces no synchronisation and can
- * stay on).  With timing enabled, every step records an event before its
- * first kernel and after each of its three kernels, on the handle's stream;
- * each of the last 64 steps keeps its own events.
+ * stay on).  With timing enabled, every step records four events on the
+ * handle's stream, around its three phases; each of the last 64 steps keeps
+ * its own events.  Events between kernels keep a kernel from launching while
+ * the one before it drains, so a monitored step can be a little slower.
  *
  *   lamb_set_timing    enable != 0 turns the monitor on (creating the events),
  *                      0 turns it off
  *   lamb_step_kernel_times  ms[0..3) receive the device durations, in
- *                      milliseconds, of step seq's grad-norm, moments and
- *                      apply kernels, waiting for them if needed
+ *                      milliseconds, of step seq's phases, waiting for them
+ *                      if needed: the grad-norm kernel, the moments kernel
+ *                      (or the fused moments-and-apply kernel), the apply
+ *                      kernel (0 when fused); in speculative mode 0, the
+ *                      one-pass kernel and the redo kernel
  *                      (LAMB_ERR_INVALID if that step was not timed or is
  *                      older than the last 64)
  *   lamb_kernel_times  the same for the last step enqueued

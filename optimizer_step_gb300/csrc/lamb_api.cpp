@@ -165,9 +165,6 @@ bool check_step_args(lamb_handle* h, const void* const* grads, float lr, float c
   return true;
 }
 
-// Enqueues one step (arguments already checked) on the handle's stream: the
-// grad pointers if new, the three kernels, and the event of its result slot.
-// t_host >= 1 fixes the step number; 0 takes it from the device counter.
 // Clears the result-ring slot of step seq before the step is enqueued.  If
 // the step that used the slot last (seq - 64) has not finished on the GPU,
 // waits for it first.
@@ -247,8 +244,11 @@ int wait_for_snapshot(lamb_handle* h) {
 }
 
 // Enqueues one step (arguments already checked) on the handle's stream: the
-// grad pointers if new, the three kernels, and the event of its result slot.
-// t_host >= 1 fixes the step number; 0 takes it from the device counter.
+// grad pointers if new, the step's kernels (grad norm, then the fused
+// moments-and-apply kernel or the moments and apply kernels; in speculative
+// mode the one-pass kernel and the redo kernel), and the event of its result
+// slot.  t_host >= 1 fixes the step number; 0 takes it from the device
+// counter.
 int enqueue_step(lamb_handle* h, const void* const* grads, float lr, int64_t t_host, float clip,
                  float loss_scale, int64_t* seq_out) {
   cudaError_t ce;

@@ -1,4 +1,4 @@
-// The three kernels of one LAMB step on sm_103a.
+// The kernels of one LAMB step on sm_103a.
 //
 // LAMB (You et al., ICLR 2020) as adopted by MegaScale ("MegaScale: Scaling
 // Large Language Model Training to More Than 10,000 GPUs", guided-reading
@@ -11,8 +11,9 @@
 // The exact method needs three passes, because r needs the global clip factor
 // and the update needs the whole tensor's ||r||:
 //   A  grad_norm_kernel  reads g (2 B/elem): sum of g^2, inf/NaN flag, one
-//      partial per CTA; its last CTA (atomic ticket, no waiting) forms ||g/S||,
-//      the clip factor and the skip flag on the device.
+//      partial per CTA; its last CTA (atomic ticket, no waiting) publishes the
+//      step: ||g/S||, the clip factor, the skip flag, t and the bias
+//      corrections.
 //   B  moments_kernel    reads g, m, v, w and writes m, v (22 B/elem); forms
 //      per-tensor sum w^2 and sum r^2; the last CTA of each tensor (ticket)
 //      turns them into trust_i.
@@ -20,6 +21,12 @@
 //      bulk copies) and writes w and the bf16 copy (18 B/elem); r is
 //      recomputed with the same function as in B, so the r applied is
 //      bit-identical to the r whose norm was taken.
+// On a shard of few waves of work items, B and C run as one persistent
+// kernel (moments_kernel<DT, true, false>): apply items follow the moments
+// items from the same counter and wait, bounded, for their tensor's trust
+// ratio.  In the opt-in speculative mode (a second m/v buffer set) one kernel
+// (spec_step_kernel) does A and B in one read of the inputs and then C, and a
+// redo kernel repeats B and C for a step that turns out clipped.
 // Small tensors (packs) are finished inside B by the warp that owns them, and
 // tensors of a single work item (at most one chunk) by the CTA that owns it,
 // so they cost 30 B/elem instead of 42: the second pass over them hits cache.
@@ -28,12 +35,12 @@
 //
 // Work is split by the host-built table of work items (chunks of large
 // tensors; packs of small tensors, a warp per tensor).  Grids are persistent
-// (a few CTAs per SM): the grad-norm kernel's CTAs walk items blockIdx.x,
-// blockIdx.x + gridDim.x, ...; the moments and apply kernels take items
-// greedily from an atomic counter, which balanced better on GB300, the
-// moments kernel from the table's start and the apply kernel from its end (so
-// each starts where the other left data in L2).  Every reduction has a fixed
-// order, so results are deterministic run to run.
+// (a few CTAs per SM): the grad-norm kernel's CTAs walk sub-items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the other kernels take items greedily from an
+// atomic counter, which balanced better on GB300, the moments pass from the
+// table's start and the separate apply kernel from its end (so each starts
+// where the other left data in L2).  Every reduction has a fixed order, so
+// results are deterministic run to run.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -67,7 +74,7 @@ namespace {
 // Resident CTAs per SM the persistent grids use (at most what fits): more
 // concurrent streams per SM than this measured slower on GB300.
 #ifndef LAMB_CTAS_PER_SM_A
-#define LAMB_CTAS_PER_SM_A 4
+#define LAMB_CTAS_PER_SM_A 3
 #endif
 #ifndef LAMB_CTAS_PER_SM_B
 #define LAMB_CTAS_PER_SM_B 3
@@ -211,35 +218,47 @@ __device__ __forceinline__ uint32_t nonfinite2(uint32_t x) {
 // fp16 grads never take the fp64 path.  (Choosing per pair instead, with
 // fp64 code inline, let the compiler predicate that code into every pair,
 // which made the grad-norm kernel twelve times slower on GB300.)
+// The fast path also leaves the inf/NaN test to the rare path: an inf or NaN
+// grad makes its fp32 partial inf or NaN, which is never inside the range,
+// so the words of such a partial are tested there, exactly.
 template <int DT>
 __device__ __forceinline__ bool partial_out_of_range(float acc, uint32_t any_bits) {
-  if (DT != LAMB_GRAD_BF16) return false;
-  return !(acc <= 0x1p120f && (acc >= 0x1p-90f || (any_bits & 0x7FFF7FFFu) == 0u));
+  if (!(acc <= 0x1p120f)) return true;  // overflow, inf or NaN
+  return DT == LAMB_GRAD_BF16 && acc < 0x1p-90f && (any_bits & 0x7FFF7FFFu) != 0u;
 }
 
-// The squares of the eight grads in four words, in fp64 (the rare path; not
-// inlined, and given the words by value, so that the fast path keeps its
-// words in registers and carries no fp64 code).
+// The squares of the eight grads in four words, in fp64, and their inf/NaN
+// flag (the rare path; not inlined, and given the words by value, so that the
+// fast path keeps its words in registers and carries no fp64 code).
+struct SquaresFp64 {
+  double sq;
+  uint32_t bad;
+};
+
 template <int DT>
-__device__ __noinline__ double squares8_fp64(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+__device__ __noinline__ SquaresFp64 squares8_fp64(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   const uint32_t w[4] = {a, b, c, d};
-  double t = 0.0;
+  SquaresFp64 r{0.0, 0u};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = decode2<DT>(w[i]);
-    t = fma(double(f.x), double(f.x), t);
-    t = fma(double(f.y), double(f.y), t);
+    r.sq = fma(double(f.x), double(f.x), r.sq);
+    r.sq = fma(double(f.y), double(f.y), r.sq);
+    r.bad |= nonfinite2<DT>(w[i]);
   }
-  return t;
+  return r;
 }
 
-// The same for 4 * K words of a trip (K vectors).
+// The same for the 4 * K words of a trip (K vectors); ORs the inf/NaN flag.
 template <int DT, int K>
-__device__ __forceinline__ double trip_squares_fp64(const uint32_t (&w)[4 * K]) {
+__device__ __forceinline__ double trip_squares_fp64(const uint32_t (&w)[4 * K], uint32_t& bad) {
   double t = 0.0;
 #pragma unroll
-  for (int u = 0; u < K; ++u)
-    t += squares8_fp64<DT>(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+  for (int u = 0; u < K; ++u) {
+    const SquaresFp64 r = squares8_fp64<DT>(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    t += r.sq;
+    bad |= r.bad;
+  }
   return t;
 }
 
@@ -369,10 +388,9 @@ __device__ __forceinline__ void sumsq_range(const uint16_t* __restrict__ g, int6
       const float2 f = decode2<DT>(w[j]);
       acc = __fmaf_rn(f.x, f.x, acc);
       acc = __fmaf_rn(f.y, f.y, acc);
-      any |= w[j];
-      bad |= nonfinite2<DT>(w[j]);
+      if (DT == LAMB_GRAD_BF16) any |= w[j];
     }
-    total += partial_out_of_range<DT>(acc, any) ? trip_squares_fp64<DT, kLoadsA>(w)
+    total += partial_out_of_range<DT>(acc, any) ? trip_squares_fp64<DT, kLoadsA>(w, bad)
                                                 : double(acc);
   }
   for (int64_t j = (nv << 3) + tid; j < n; j += nthr) {  // fewer than 8: fp64 squares
@@ -561,10 +579,9 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
         const float2 f = decode2<DT>(w[h]);
         acc = __fmaf_rn(f.x, f.x, acc);
         acc = __fmaf_rn(f.y, f.y, acc);
-        any |= w[h];
-        bad |= nonfinite2<DT>(w[h]);
+        if (DT == LAMB_GRAD_BF16) any |= w[h];
       }
-      total += partial_out_of_range<DT>(acc, any) ? trip_squares_fp64<DT, kLoadsA>(w)
+      total += partial_out_of_range<DT>(acc, any) ? trip_squares_fp64<DT, kLoadsA>(w, bad)
                                                   : double(acc);
     }
     // The last (fewer than 8) elements of each staged sub-item: one thread
@@ -685,16 +702,18 @@ __device__ __forceinline__ void moments_range_io(const float* mi, const float* v
           if (G2) {
             pv = __fmaf_rn(f.x, f.x, pv);
             pv = __fmaf_rn(f.y, f.y, pv);
-            bad |= nonfinite2<DT>(wv[j]);
           }
           e.moments(f.x, mr[u][2 * j], vr[u][2 * j]);
           e.moments(f.y, mr[u][2 * j + 1], vr[u][2 * j + 1]);
         }
         if (G2) {  // this vector's squares: fp32, or fp64 when out of range
-          if (partial_out_of_range<DT>(pv, wv[0] | wv[1] | wv[2] | wv[3]))
-            sgd += squares8_fp64<DT>(wv[0], wv[1], wv[2], wv[3]);
-          else
+          if (partial_out_of_range<DT>(pv, wv[0] | wv[1] | wv[2] | wv[3])) {
+            const SquaresFp64 r = squares8_fp64<DT>(wv[0], wv[1], wv[2], wv[3]);
+            sgd += r.sq;
+            bad |= r.bad;
+          } else {
             sg = __fadd_rn(sg, pv);
+          }
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {

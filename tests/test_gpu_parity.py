@@ -147,6 +147,66 @@ def test_dynamic_loss_scaler_matches_the_oracle():
         assert opt.step(wl.lr, t, 0.0, 1024.0)[0] is False and opt.loss_scale == 1024.0
 
 
+class _DeviceFloat:
+    """One fp32 at a device address, for torch.as_tensor (CUDA array interface)."""
+
+    def __init__(self, ptr):
+        self.__cuda_array_interface__ = {"shape": (1,), "typestr": "<f4", "data": (ptr, False),
+                                         "version": 3}
+
+
+def test_async_steps_with_the_loss_scale_read_on_the_device():
+    """A caller that never waits: fp16 grads are scaled on the GPU by the
+    scale lamb_loss_scale_device exposes (in stream order, before each
+    step_async), the scale backs off after overflows and grows after clean
+    steps; the outcomes read later follow the oracle's scaler rule."""
+    wl = custom([300000, 4096, 77], grad_dtype=torch.float16, t0=1, warm=False, S=1.0)
+    st = W.make_state(wl, "cuda")
+    cfg = dict(growth=2.0, backoff=0.5, growth_interval=2, min_scale=1.0, max_scale=2.0 ** 24)
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, grad_dtype=torch.float16) as opt:
+        opt.set_loss_scaler(init_scale=2.0 ** 22, growth_factor=2.0, backoff_factor=0.5,
+                            growth_interval=2, min_scale=1.0, max_scale=2.0 ** 24)
+        opt.set_step(1)
+        scale_dev = torch.as_tensor(_DeviceFloat(opt.loss_scale_device_ptr()), device="cuda")
+        raw = [W.make_grads(custom([300000, 4096, 77], grad_dtype=torch.float32, seed=50 + k,
+                                   sigma=1e-3), 1, "cuda")[1] for k in range(8)]
+        bufs, seqs = [], []
+        for k in range(8):  # every step's grads = raw * (the scale on the GPU), no host wait
+            g = [(x * scale_dev).to(torch.float16) for x in raw[k]]
+            bufs.append(g)
+            seqs.append(opt.step_async(wl.lr, 0.0, 1.0, grads=opt.prepare_grads(g)))
+        outs = [opt.result(q) for q in seqs]
+        scale, good = 2.0 ** 22, 0
+        for k, (sk, gn, t) in enumerate(outs):
+            g_host = [W.as_bits(x) for x in bufs[k]]
+            bad = any(not np.isfinite(oracle.decode_grad(b, oracle.GRAD_FP16)).all()
+                      for b in g_host)
+            assert sk == bad, (k, sk, bad)
+            scale, good = oracle.loss_scale_update(scale, good, int(bad), **cfg)
+        torch.cuda.synchronize()
+        assert scale_dev.item() == scale and opt.next_loss_scale == scale
+        assert sum(o[0] for o in outs) >= 1 and not all(o[0] for o in outs)
+
+
+def test_info_reports_the_kernels_a_step_runs():
+    """Few waves of work items: one fused moments-and-apply kernel; many: two."""
+    for sizes, fused in (([70001, 5000, 300], 1), ([1 << 27, 5000], 0)):
+        wl = custom(sizes)
+        st = W.make_state(wl, "cuda")
+        with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags) as opt:
+            info = opt.info()
+            assert info["fused"] == fused and info["speculative"] == 0
+            assert info["n_params"] == sum(sizes)
+            one_pass_max = max(4096, info["chunk_elems"])  # packed, or a single work item
+            assert info["one_pass_params"] == sum(n for n in sizes if n <= one_pass_max)
+            _, gv = W.make_grads(wl, 1, "cuda")
+            opt.set_timing(True)
+            assert opt.step(wl.lr, 1, 0.0, 1.0, grads=gv)[0] is False
+            ms = opt.kernel_times()
+            assert ms[0] > 0 and ms[1] > 0 and (ms[2] == pytest.approx(0.0, abs=0.02) if fused
+                                                 else ms[2] > 0)
+
+
 @pytest.mark.parametrize("pinned", [True, False])
 def test_snapshot_captures_the_state_between_steps(pinned):
     """A snapshot taken after step 2 holds exactly the state after step 2, even
