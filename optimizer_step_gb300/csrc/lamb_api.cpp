@@ -273,17 +273,17 @@ int enqueue_step(lamb_handle* h, const void* const* grads, float lr, int64_t t_h
     rc = launch_spec_redo(h->T, h->grid[1], h->hp.grad_dtype, hy, h->stream);
     if (rc) return cuda_fail(cudaError_t(rc), "redo kernel launch");
   } else {
-  rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, na, sa, h->stream);
-  if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
-  if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
-  if ((ce = mark(h, r, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->fused, h->stream);
-  if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
-  if ((ce = mark(h, r, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
-  if (!h->fused) {
-    rc = launch_apply(h->T, h->grid[2], hy, h->stream);
-    if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
-  }
+    rc = launch_grad_norm(h->T, h->grid[0], h->hp.grad_dtype, na, sa, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "grad-norm kernel launch");
+    if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
+    if ((ce = mark(h, r, 1)) != cudaSuccess) return cuda_fail(ce, "event record");
+    rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, hy, h->fused, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
+    if ((ce = mark(h, r, 2)) != cudaSuccess) return cuda_fail(ce, "event record");
+    if (!h->fused) {
+      rc = launch_apply(h->T, h->grid[2], hy, h->stream);
+      if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+    }
   }
   if ((ce = mark(h, r, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
   if ((ce = cudaEventRecord(h->ring_ev[r], h->stream)) != cudaSuccess)
