@@ -185,9 +185,9 @@ LAMB_API int lamb_create(lamb_handle** out, int32_t n_tensors, const int64_t* si
  *                 before summing), to be summed over the group in place
  *
  * A handle made by lamb_create has neither buffer and cannot take split
- * steps; one made here takes ordinary steps too (a tensor with an exchange
- * slot then gets its trust ratio from tensor_exchange as summed before the
- * apply phase, so ordinary steps make sense only for a group of one rank).
+ * steps.  One made here takes ordinary steps (lamb_step, lamb_step_async) only
+ * while no tensor has an exchange slot; with one, they return
+ * LAMB_ERR_INVALID, since a shared tensor's trust ratio needs the group's sums.
  */
 LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int64_t* sizes,
                                  const uint8_t* wd_flags, float* const* w, float* const* m,

@@ -133,6 +133,19 @@ void release(lamb_handle* h) {
   h->dev_block = nullptr;
 }
 
+// Ordinary steps need every trust ratio from this shard alone: none may be
+// shared with other ranks.
+bool check_unshared(lamb_handle* h, int* rc) {
+  for (const TensorDesc& d : h->td_host) {
+    if (d.xslot >= 0) {
+      *rc = fail(LAMB_ERR_INVALID, "the shard has tensors shared with other ranks: step it "
+                                   "with the split step");
+      return false;
+    }
+  }
+  return true;
+}
+
 bool check_step_args(lamb_handle* h, const void* const* grads, float lr, float clip,
                      float loss_scale, int* rc) {
   if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale)) {
@@ -571,7 +584,7 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
   if (!out) return fail(LAMB_ERR_INVALID, "out is NULL");
   if (t < 1) return fail(LAMB_ERR_INVALID, "t must be >= 1");
   int rc = LAMB_OK;
-  if (!check_step_args(h, grads, lr, clip, loss_scale, &rc)) return rc;
+  if (!check_unshared(h, &rc) || !check_step_args(h, grads, lr, clip, loss_scale, &rc)) return rc;
   std::memset(out, 0, sizeof *out);
   out->loss_scale = loss_scale;
   out->next_loss_scale = loss_scale;
@@ -592,7 +605,7 @@ LAMB_API int lamb_step_async(lamb_handle* h, const void* const* grads, float lr,
   if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
   if (h->split_phase != 0) return fail(LAMB_ERR_INVALID, "a split step is in progress");
   int rc = LAMB_OK;
-  if (!check_step_args(h, grads, lr, clip, loss_scale, &rc)) return rc;
+  if (!check_unshared(h, &rc) || !check_step_args(h, grads, lr, clip, loss_scale, &rc)) return rc;
   DeviceGuard dg(h->device);
   if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
   int64_t s = 0;

@@ -24,7 +24,7 @@ import pytest
 import torch
 
 import workloads as W
-from optimizer_step_gb300 import Lamb
+from optimizer_step_gb300 import Lamb, LambError
 
 from parity import HostState, assert_close, compare_state, oracle_step, rtol_for
 
@@ -141,6 +141,35 @@ def test_split_step_with_a_tensor_over_three_ranks_and_fp16_scale():
     finally:
         for opt, _, _, _ in ranks:
             opt.close()
+
+
+def test_ordinary_steps_are_refused_while_a_tensor_is_shared():
+    """A shared tensor's trust ratio needs the group's sums, so lamb_step and
+    lamb_step_async refuse such a shard (before enqueueing anything); a shard
+    of the same kind whose tensors are all whole still takes them."""
+    wl = _workload()
+    st = W.make_state(wl, "cuda")
+    _, gviews = W.make_grads(wl, 1, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, 2)
+    opt, _, _, g = _rank_handle(wl, st, gviews, pieces[0], slots[0], 1, "cuda")
+    before = [x.clone() for x in (st.w_flat, st.m_flat, st.v_flat)]
+    try:
+        assert any(k >= 0 for k in slots[0])
+        with pytest.raises(LambError, match="shared with other ranks"):
+            opt.step(wl.lr, wl.t0, wl.clip, wl.loss_scale, grads=g)
+        with pytest.raises(LambError, match="shared with other ranks"):
+            opt.step_async(wl.lr, wl.clip, grads=g)
+    finally:
+        opt.close()
+    torch.cuda.synchronize()
+    for a, b in zip(before, (st.w_flat, st.m_flat, st.v_flat)):
+        assert torch.equal(a, b)
+    whole = [(i, 0, n) for i, n in enumerate(wl.sizes)]
+    opt, _, _, g = _rank_handle(wl, st, gviews, whole, [-1] * len(whole), 0, "cuda")
+    try:
+        assert opt.step(wl.lr, wl.t0, wl.clip, wl.loss_scale, grads=g)[0] is False
+    finally:
+        opt.close()
 
 
 # ------------------------------------------------ two processes, gloo sums
