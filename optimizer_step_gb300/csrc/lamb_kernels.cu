@@ -419,35 +419,62 @@ __device__ __forceinline__ void write_record(const StepScalars* sc, ResultRecord
 // data-parallel group) and the inf/NaN flag: the grad norm ||g/S||, the clip
 // factor, the skip flag, the step number t and its bias corrections (from
 // beta^t in fp64, rounded once to fp32; t and beta^t advance only on a step
-// that is not skipped -- fp64 is slow on GB300, so there is no pow here), the
-// dynamic loss scale, the host's copy of the outcome, and the item counters
-// of the next step.  One thread.
+// that is not skipped), the dynamic loss scale, the host's copy of the
+// outcome, and the item counters of the next step.
+//
+// Called by all 32 lanes of one warp with the same arguments; lane 0 writes
+// and its return value (clipped) is the one to use.  fp64 is slow on GB300
+// (a division takes about half a microsecond on one thread, and this runs on
+// the step's critical path), so the five divisions run at once, one per lane,
+// and there is no pow: ||g/S|| = sqrt(s)/S; the clipped grad factor
+// c/S = (clip/||g/S||)/S, taken as clip/sqrt(s) (equal up to rounding); the
+// unclipped one 1/S; and 1/(1-beta1^t), 1/(1-beta2^t).
 __device__ bool publish_step(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, double s,
-                             bool nf) {
+                             bool nf, int lane) {
   StepScalars* sc = T.sc;
   const float S = sa.dynamic ? sc->scale : sa.fixed;
   const double loss_scale = double(S);
+  const bool host_t = na.t_host > 0;
+  const int64_t t = host_t ? na.t_host : sc->t_next;
+  const double p1 = host_t ? na.p1_host : sc->p1_next;  // beta1^t
+  const double p2 = host_t ? na.p2_host : sc->p2_next;  // beta2^t
+  const double rs = sqrt(s);
+  double num = 1.0, den = 1.0;
+  if (lane == 0) {
+    num = rs;
+    den = loss_scale;
+  } else if (lane == 1) {
+    num = double(na.clip);
+    den = rs;
+  } else if (lane == 2) {
+    den = loss_scale;
+  } else if (lane == 3) {
+    den = 1.0 - p1;
+  } else if (lane == 4) {
+    den = 1.0 - p2;
+  }
+  const double q = num / den;
+  const double gn = __shfl_sync(0xffffffffu, q, 0);
+  const double clip_gscale = __shfl_sync(0xffffffffu, q, 1);
+  const double inv_scale = __shfl_sync(0xffffffffu, q, 2);
+  const double c1 = __shfl_sync(0xffffffffu, q, 3);
+  const double c2 = __shfl_sync(0xffffffffu, q, 4);
+  if (lane != 0) return false;
   bool clipped = false;
   if (nf) {
     sc->skip = 1;
     sc->grad_norm = __longlong_as_double(0x7FF0000000000000ll);  // +inf
     sc->gscale = 0.0f;
   } else {
-    const double gn = sqrt(s) / loss_scale;
     clipped = na.clip > 0.0f && gn > double(na.clip);
-    const double c = clipped ? double(na.clip) / gn : 1.0;
     sc->skip = 0;
     sc->grad_norm = gn;
-    sc->gscale = float(c / loss_scale);
+    sc->gscale = float(clipped ? clip_gscale : inv_scale);
   }
   sc->scale_used = S;
-  const bool host_t = na.t_host > 0;
-  const int64_t t = host_t ? na.t_host : sc->t_next;
-  const double p1 = host_t ? na.p1_host : sc->p1_next;  // beta1^t
-  const double p2 = host_t ? na.p2_host : sc->p2_next;  // beta2^t
   sc->t_used = t;
-  sc->c1 = float(1.0 / (1.0 - p1));
-  sc->c2 = float(1.0 / (1.0 - p2));
+  sc->c1 = float(c1);
+  sc->c2 = float(c2);
   sc->t_next = nf ? t : t + 1;
   sc->p1_next = nf ? p1 : p1 * double(na.b1);
   sc->p2_next = nf ? p2 : p2 * double(na.b2);
@@ -624,24 +651,30 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
   double s = 0.0;
   for (int32_t i = threadIdx.x; i < int32_t(gridDim.x); i += kThreads) s += __ldcg(&T.item_g2[i]);
   s = block_sum(s, red);
-  if (threadIdx.x == 0) {
-    const uint32_t nf = atomicExch(&T.sc->nonfinite, 0u);
+  if (warp != 0) return;
+  uint32_t nf = 0;
+  if (lane == 0) {
+    nf = atomicExch(&T.sc->nonfinite, 0u);
     T.sc->ticket = 0u;  // ready for the next step
-    if (na.partial) {
-      // Split step: this shard's partials go out to be summed over the group;
-      // the finalize kernel publishes the step once they come back.
+  }
+  nf = __shfl_sync(0xffffffffu, nf, 0);
+  if (na.partial) {
+    // Split step: this shard's partials go out to be summed over the group;
+    // the finalize kernel publishes the step once they come back.
+    if (lane == 0) {
       T.xn[0] = s;
       T.xn[1] = nf ? 1.0 : 0.0;
-    } else {
-      publish_step(T, na, sa, s, nf != 0u);
     }
+  } else {
+    publish_step(T, na, sa, s, nf != 0u, lane);
   }
 }
 
 // Split step: the group's summed {sum of raw g^2, inf/NaN count} -> the
 // step's scalars, exactly as the grad-norm kernel's last CTA forms them.
 __global__ void finalize_kernel(DevTables T, NormArgs na, ScaleArgs sa) {
-  if (threadIdx.x == 0) publish_step(T, na, sa, T.xn[0], !(T.xn[1] == 0.0));
+  // one warp (publish_step's lanes)
+  publish_step(T, na, sa, T.xn[0], !(T.xn[1] == 0.0), int(threadIdx.x & 31));
 }
 
 // Split step: trust ratio of each tensor shared with other ranks, from the
@@ -1158,17 +1191,23 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) spec_step_kernel(D
         double g2 = 0.0;
         for (int32_t k = threadIdx.x; k < n; k += kThreads) g2 += __ldcg(&T.item_g2[k]);
         g2 = block_sum(g2, red1);
-        if (threadIdx.x == 0) {
-          const uint32_t nf = atomicExch(&sc->nonfinite, 0u);
-          sc->items_done = 0u;
+        if (warp == 0) {
+          uint32_t nf = 0;
+          if (lane == 0) {
+            nf = atomicExch(&sc->nonfinite, 0u);
+            sc->items_done = 0u;
+          }
+          nf = __shfl_sync(0xffffffffu, nf, 0);
           const int32_t cur = sc->cur;
-          const bool clipped = publish_step(T, na, sa, g2, nf != 0u);
-          sc->src = cur;
-          sc->spec_ok = (!nf && !clipped) ? 1 : 0;
-          sc->cur = nf ? cur : 1 - cur;
-          __threadfence();
-          st_release(&sc->published, hp.tag);
-          if (na.slot) static_cast<volatile ResultRecord*>(na.slot)->state_buf = sc->cur;
+          const bool clipped = publish_step(T, na, sa, g2, nf != 0u, lane);
+          if (lane == 0) {
+            sc->src = cur;
+            sc->spec_ok = (!nf && !clipped) ? 1 : 0;
+            sc->cur = nf ? cur : 1 - cur;
+            __threadfence();
+            st_release(&sc->published, hp.tag);
+            if (na.slot) static_cast<volatile ResultRecord*>(na.slot)->state_buf = sc->cur;
+          }
         }
       }
       continue;

@@ -85,6 +85,36 @@ def test_nonfinite_grad_skips_bit_exactly(grad_dtype, kind):
     opt.close()
 
 
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_power_of_two_loss_scale_is_bit_exact(grad_dtype, clip):
+    """Grads multiplied by 2^4 and stepped with S = 2^4 give the same state,
+    bit for bit, as the grads stepped with S = 1, clipped or not (the scaling
+    is exact in bf16 and fp16 at these magnitudes, and so is every product
+    with the grad factor); the grad norm is the same number too."""
+    k = 16.0
+    wl = custom([5000, 70001, 300, 131072, 7], grad_dtype=grad_dtype, t0=3, clip=clip)
+    _, gv = W.make_grads(wl, 1, "cuda")
+    gv2 = [(g.float() * k).to(grad_dtype) for g in gv]
+    for a, b in zip(gv, gv2):
+        assert torch.equal((b.float() / k).to(grad_dtype).view(torch.int16), a.view(torch.int16))
+    outs = []
+    for grads, S in ((gv, 1.0), (gv2, k)):
+        st = W.make_state(wl, "cuda")
+        with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, grad_dtype=grad_dtype) as opt:
+            sk, gn = opt.step(wl.lr, wl.t0, clip, S, grads=grads)
+            sk2, gn2 = opt.step(wl.lr, wl.t0 + 1, clip, S, grads=grads)
+        assert not sk and not sk2
+        outs.append(((gn, gn2), [x.clone() for x in (st.w_flat, st.m_flat, st.v_flat,
+                                                        st.w16_flat)]))
+    (n1, s1), (n2, s2) = outs
+    assert n1 == n2
+    if clip:
+        assert n1[0] > clip  # the clip factor is in play
+    for a, b in zip(s1, s2):
+        assert torch.equal(a.view(torch.int8), b.view(torch.int8))
+
+
 def test_rotating_grad_buffers_match_the_oracle():
     """Steps that take their grads from 5 different buffers in turn (more
     buffers than the handle's grad-pointer slots) still match the oracle."""
