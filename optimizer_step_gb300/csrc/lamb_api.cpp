@@ -82,6 +82,7 @@ struct lamb_handle {
   cudaEvent_t ring_ev[kResultRing] = {};  // recorded after each step's last kernel
   int64_t next_seq = 0;            // sequence number of the next step
   int32_t split_a = 1;             // grad-norm sub-items per chunk item
+  bool has_shared = false;         // some tensor has an exchange slot (split steps only)
   int64_t chunk = 0;               // chunk size of the work table
   bool fused = false;              // ordinary steps: moments and apply in one kernel
   bool spec = false;               // speculative mode: second m, v buffers given
@@ -136,14 +137,10 @@ void release(lamb_handle* h) {
 // Ordinary steps need every trust ratio from this shard alone: none may be
 // shared with other ranks.
 bool check_unshared(lamb_handle* h, int* rc) {
-  for (const TensorDesc& d : h->td_host) {
-    if (d.xslot >= 0) {
-      *rc = fail(LAMB_ERR_INVALID, "the shard has tensors shared with other ranks: step it "
-                                   "with the split step");
-      return false;
-    }
-  }
-  return true;
+  if (!h->has_shared) return true;
+  *rc = fail(LAMB_ERR_INVALID, "the shard has tensors shared with other ranks: step it with "
+                               "the split step");
+  return false;
 }
 
 bool check_step_args(lamb_handle* h, const void* const* grads, float lr, float clip,
@@ -457,6 +454,7 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
     td[i].first_item = h->plan.first_item[i];
     td[i].n_items = h->plan.n_items[i];
     td[i].xslot = exchange_slot ? exchange_slot[i] : -1;
+    if (td[i].xslot >= 0) h->has_shared = true;
     td[i].m2 = nullptr;
     td[i].v2 = nullptr;
   }
