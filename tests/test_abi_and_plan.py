@@ -105,6 +105,25 @@ def test_plan_covers_every_element_once(sizes, chunk):
     check_plan(sizes, chunk)
 
 
+def test_plan_properties_on_random_tensor_lists():
+    """The work table's invariants (check_plan) on random tensor lists that
+    mix empty, packed, one-chunk and many-chunk tensors and sizes next to the
+    pack and chunk limits, for every kind of chunk size."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+    lim = og.plan_limits()
+    edges = [0, 1, 7, 8, 9, lim["small_max"] - 1, lim["small_max"], lim["small_max"] + 1,
+             2047, 2048, 2049, 32767, 32768, 32769, 65536 + 7]
+    size = st.one_of(st.sampled_from(edges), st.integers(0, 20), st.integers(0, 300000))
+
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True)
+    @hyp.given(st.lists(size, max_size=60), st.sampled_from([0, 2048, 4096, 12288, 32768]))
+    def prop(sizes, chunk):
+        check_plan(sizes, chunk)
+
+    prop()
+
+
 def test_plan_ragged_config():
     import workloads
     wl = workloads.ragged()

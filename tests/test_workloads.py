@@ -3,6 +3,7 @@ counts, draws are reproducible, and planted inf/NaN land where stated."""
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import workloads as W
@@ -61,9 +62,49 @@ def test_student_t_has_heavy_tails():
     assert kurt > 6  # a normal has 3; t(3) has infinite kurtosis
 
 
+def _check_zero2(sizes, n_ranks):
+    pieces, slots = W.zero2_pieces(sizes, n_ranks)
+    assert len(pieces) == len(slots) == n_ranks
+    seen = [np.zeros(n, np.int32) for n in sizes]
+    at = 0  # pieces are the flattened state, in order, rank after rank
+    for mine, sl in zip(pieces, slots):
+        assert len(mine) == len(sl)
+        for (i, b, e), k in zip(mine, sl):
+            assert 0 <= b < e <= sizes[i]
+            assert b % 8 == 0
+            flat = sum(sizes[:i]) + b
+            assert flat == at
+            at = flat + (e - b)
+            seen[i][b:e] += 1
+            assert (k == -1) == (b == 0 and e == sizes[i])
+    assert at == sum(sizes)
+    assert all((x == 1).all() for x in seen)
+    slot_of = {}
+    for mine, sl in zip(pieces, slots):
+        for (i, _, _), k in zip(mine, sl):
+            if k >= 0:
+                assert slot_of.setdefault(i, k) == k
+    assert sorted(slot_of.values()) == list(range(len(slot_of)))
+
+
+def test_zero2_pieces_on_random_tensor_lists():
+    """The same properties on random tensor lists (empty tensors included)
+    and group sizes: the pieces tile the flattened state in order."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=200, deadline=None, derandomize=True)
+    @hyp.given(st.lists(st.integers(0, 50000), min_size=1, max_size=25), st.integers(1, 9))
+    def prop(sizes, n_ranks):
+        _check_zero2(sizes, n_ranks)
+
+    prop()
+
+
 def test_zero2_pieces_cover_every_element_once_with_aligned_cuts():
     sizes = [5000, 70001, 300, 200003, 17, 4096, 40000]
     for n_ranks in (1, 2, 3, 5, 8):
+        _check_zero2(sizes, n_ranks)
         pieces, slots = W.zero2_pieces(sizes, n_ranks)
         seen = [np.zeros(n, np.int32) for n in sizes]
         for mine, sl in zip(pieces, slots):
