@@ -221,7 +221,10 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
  *       step's sequence number for lamb_step_result.
  *
  * The calls must come in this order (LAMB_ERR_INVALID otherwise, with nothing
- * enqueued); no other step may start on the handle in between.  The result of
+ * enqueued).  In between, the handle refuses (LAMB_ERR_INVALID) every call
+ * that would start another step or change what this one reads or copies:
+ * lamb_step, lamb_step_async, lamb_set_step, lamb_set_loss_scaler,
+ * lamb_set_speculative and lamb_snapshot_async.  The result of
  * a group of one rank, with no exchange at all, equals lamb_step's.
  */
 LAMB_API int lamb_split_norms(lamb_handle* h, const void* const* grads, float loss_scale);

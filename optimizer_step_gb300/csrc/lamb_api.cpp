@@ -134,6 +134,14 @@ void release(lamb_handle* h) {
   h->dev_block = nullptr;
 }
 
+// Calls that change what a step reads, or copy the state, must not fall
+// between the phases of a split step.
+bool check_no_split(lamb_handle* h, int* rc) {
+  if (h->split_phase == 0) return true;
+  *rc = fail(LAMB_ERR_INVALID, "a split step is in progress");
+  return false;
+}
+
 // Ordinary steps need every trust ratio from this shard alone: none may be
 // shared with other ranks.
 bool check_unshared(lamb_handle* h, int* rc) {
@@ -802,10 +810,12 @@ LAMB_API int lamb_set_step(lamb_handle* h, int64_t t) {
   g_last_error.clear();
   if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
   if (t < 1) return fail(LAMB_ERR_INVALID, "t must be >= 1");
+  int rc = LAMB_OK;
+  if (!check_no_split(h, &rc)) return rc;
   DeviceGuard dg(h->device);
   if (!dg.ok) return fail(LAMB_ERR_CUDA, "cannot make the handle's device current");
-  const int rc = launch_set_step(h->T.sc, t, std::pow(double(h->hp.beta1), double(t)),
-                                 std::pow(double(h->hp.beta2), double(t)), h->stream);
+  rc = launch_set_step(h->T.sc, t, std::pow(double(h->hp.beta1), double(t)),
+                       std::pow(double(h->hp.beta2), double(t)), h->stream);
   return rc ? cuda_fail(cudaError_t(rc), "setting the step number") : LAMB_OK;
 }
 
@@ -819,6 +829,8 @@ LAMB_API int lamb_loss_scale_device(lamb_handle* h, const float** scale) {
 LAMB_API int lamb_set_loss_scaler(lamb_handle* h, const lamb_loss_scaler* cfg) {
   g_last_error.clear();
   if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  int rc = LAMB_OK;
+  if (!check_no_split(h, &rc)) return rc;
   if (!cfg) {
     h->scaler = ScaleArgs{};
     return LAMB_OK;
@@ -908,6 +920,8 @@ LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* co
                                  float* const* host_v, void* stream) {
   g_last_error.clear();
   if (!h) return fail(LAMB_ERR_INVALID, "handle is NULL");
+  int rc = LAMB_OK;
+  if (!check_no_split(h, &rc)) return rc;  // the state is half-updated until split_apply
   if (h->n_tensors > 0 && (!host_w || !host_m || !host_v))
     return fail(LAMB_ERR_INVALID, "host pointer arrays must be non-NULL");
   for (int32_t i = 0; i < h->n_tensors; ++i) {
@@ -932,7 +946,7 @@ LAMB_API int lamb_snapshot_async(lamb_handle* h, float* const* host_w, float* co
     return cuda_fail(ce, "ordering after the previous snapshot");
   int32_t cur = 0;  // speculative mode: the set holding the state (the host waits to learn it)
   if (h->spec) {
-    int rc = current_set(h, &cur);
+    rc = current_set(h, &cur);
     if (rc != LAMB_OK) return rc;
   }
   for (int32_t i = 0; i < h->n_tensors; ++i) {

@@ -301,12 +301,19 @@ class Lamb:
             if getattr(self, "_snap_stream", None) is None:
                 self._snap_stream = torch.cuda.Stream(device=self.device)
             stream = self._snap_stream
-        # The host tensors must outlive their copies: keep every outstanding set.
+        # The host tensors must outlive their copies: keep every outstanding set
+        # (not one the library refused before enqueueing anything).
         if getattr(self, "_snap_keep", None) is None:
             self._snap_keep = []
         self._snap_keep.append((list(host_w), list(host_m), list(host_v)))
-        check(self._lib.lamb_snapshot_async(self._h, _ptrs(host_w), _ptrs(host_m),
-                                            _ptrs(host_v), ctypes.c_void_p(stream.cuda_stream)))
+        try:
+            check(self._lib.lamb_snapshot_async(self._h, _ptrs(host_w), _ptrs(host_m),
+                                                _ptrs(host_v),
+                                                ctypes.c_void_p(stream.cuda_stream)))
+        except LambError as e:
+            if e.code in (_lib.LAMB_ERR_INVALID, _lib.LAMB_ERR_ALIGN):
+                self._snap_keep.pop()
+            raise
 
     def snapshot_wait(self) -> None:
         """Block until every outstanding snapshot is in host memory."""

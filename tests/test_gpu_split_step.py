@@ -172,6 +172,43 @@ def test_ordinary_steps_are_refused_while_a_tensor_is_shared():
         opt.close()
 
 
+def test_calls_between_the_phases_are_refused():
+    """Between lamb_split_norms and lamb_split_apply the handle refuses
+    another step, a new step number or loss scaler, speculative mode and a
+    snapshot (the state is half-updated there); the split step then finishes
+    normally."""
+    wl = _workload(clip=0.0)
+    st = W.make_state(wl, "cuda")
+    _, gviews = W.make_grads(wl, 1, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, 1)
+    opt, xn, xt, g = _rank_handle(wl, st, gviews, pieces[0], slots[0], 1, "cuda")
+    host = [torch.empty(n, dtype=torch.float32).pin_memory() for n in wl.sizes]
+    m2 = [torch.zeros_like(x) for x in st.m]
+    v2 = [torch.zeros_like(x) for x in st.v]
+    refused = {
+        "step": lambda: opt.step(wl.lr, wl.t0, 0.0, 1.0, grads=g),
+        "step_async": lambda: opt.step_async(wl.lr, 0.0, grads=g),
+        "set_step": lambda: opt.set_step(7),
+        "set_loss_scaler": lambda: opt.set_loss_scaler(),
+        "set_speculative": lambda: opt.set_speculative(m2, v2),
+        "snapshot_async": lambda: opt.snapshot_async(host, host, host),
+    }
+    try:
+        for phase in ("norms", "moments"):
+            if phase == "norms":
+                opt.split_norms(g, wl.loss_scale)
+            else:
+                opt.split_moments(wl.lr, 0.0, wl.t0)
+            for name, call in refused.items():
+                with pytest.raises(LambError, match="split step"):
+                    call()
+        seq = opt.split_apply()
+        sk, gn, t = opt.result(seq)
+        assert sk is False and math.isfinite(gn) and t == wl.t0
+    finally:
+        opt.close()
+
+
 # ------------------------------------------------ two processes, gloo sums
 def _free_port():
     with socket.socket() as s:
