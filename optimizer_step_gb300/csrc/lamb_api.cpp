@@ -68,6 +68,11 @@ static constexpr int kResultRing = 64;
 #ifndef LAMB_FUSED_MAX_WAVES
 #define LAMB_FUSED_MAX_WAVES 8
 #endif
+// A fused shard's last tensor of several chunks gets chunks 2^LAMB_TAIL_SHIFT
+// times smaller, so that the kernel's last items end closer together.
+#ifndef LAMB_TAIL_SHIFT
+#define LAMB_TAIL_SHIFT 1
+#endif
 
 struct lamb_handle {
   int device = 0;
@@ -438,7 +443,8 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
   const bool fused = !h->plan.items.empty() &&
                      int64_t(h->plan.items.size()) <=
                          int64_t(LAMB_FUSED_MAX_WAVES) * int64_t(per_sm[1]) * sms;
-  if (fused && !build_plan(n_tensors, sizes, chunk, no_pack.data(), 1, &h->plan, &err)) {
+  if (fused && !build_plan(n_tensors, sizes, chunk, no_pack.data(), LAMB_TAIL_SHIFT, &h->plan,
+                           &err)) {
     delete h;
     return fail(LAMB_ERR_INVALID, err);
   }
