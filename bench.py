@@ -91,6 +91,9 @@ def parse_args(argv=None):
     p.add_argument("--speculative", action="store_true",
                    help="speculative mode: a second set of m and v buffers, so that a step "
                         "reads the grads once (40 B/param while no step is clipped)")
+    p.add_argument("--split", action="store_true",
+                   help="the split step of a ZeRO-2 group (lamb_split_norms / _moments / "
+                        "_apply) on a group of one: every phase, no exchange to wait for")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--snapshot", action="store_true",
                    help="also time the state snapshot into pinned host memory (the first "
@@ -297,8 +300,15 @@ def run_ours(args, world, rank, local):
     N = wl.n_params
     st = W.make_state(wl, device)
     gflat, gv = W.make_grads(wl, 1, device)
+    if args.split and args.speculative:
+        raise SystemExit("--split and --speculative do not combine (split steps refuse it)")
+    split_kw = {}
+    if args.split:  # a group of one: the exchange buffers exist, no tensor is shared
+        split_kw = dict(exchange_slots=[-1] * len(wl.sizes),
+                        norm_exchange=torch.zeros(2, dtype=torch.float64, device=device),
+                        tensor_exchange=torch.zeros(2, dtype=torch.float64, device=device))
     opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, beta1=wl.beta1, beta2=wl.beta2,
-               eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype)
+               eps=wl.eps, weight_decay=wl.weight_decay, grad_dtype=wl.grad_dtype, **split_kw)
     grads0 = opt.prepare_grads(gv)
     opt.set_grads(grads0)
     if args.speculative:
@@ -312,6 +322,10 @@ def run_ours(args, world, rank, local):
     opt.set_step(wl.t0)
 
     def step():
+        if args.split:  # the group's sums are this rank's own: nothing to exchange
+            opt.split_norms(None, wl.loss_scale)
+            opt.split_moments(wl.lr, wl.clip, 0)
+            return opt.split_apply()
         return opt.step_async(wl.lr, wl.clip, wl.loss_scale)
 
     for _ in range(max(3, args.warmup)):
@@ -356,6 +370,7 @@ def run_ours(args, world, rank, local):
     opt.set_timing(False)
 
     info = opt.info()
+    fused = bool(info["fused"])  # one moments-and-apply kernel (split steps too)
     n_packed = info["one_pass_params"]
     kbytes = kernel_bytes(N, n_packed)
     step_bytes = sum(kbytes.values())
@@ -372,7 +387,7 @@ def run_ours(args, world, rank, local):
         times = {"spec_step": times["moments"], "redo": times["apply"]}
         step_bytes = statistics.mean(
             sum(spec_kernel_bytes(N, n_packed, clip_of(o)).values()) for o in outcomes)
-    elif info["fused"]:
+    elif fused:
         # One persistent kernel runs the moments and the apply passes.
         kbytes = {"grad_norm": kbytes["grad_norm"],
                   "moments_apply": kbytes["moments"] + kbytes["apply"]}
@@ -385,7 +400,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = hbm_peak()
     step_ms = sec / args.steps * 1e3
     dominant = ("spec_step" if info["speculative"] else
-                "moments_apply" if info["fused"] else "moments")
+                "moments_apply" if fused else "moments")
     achieved = kern[dominant]["GB/s"]
     # The recorded counters come from a cut of the same tensor mix; they are
     # scaled by params only while one-pass tensors are a negligible share.
@@ -504,10 +519,13 @@ def run_ours(args, world, rank, local):
                                                  1e9, 1),
                          "floor_28B_frac_of_peak": round(FLOOR_BYTES_PER_PARAM * N /
                                                          (step_ms / 1e3) / 1e9 / peak, 4)},
-            "gpu_launches": (2 if info["fused"] or info["speculative"] else 3) * args.steps,
+            # split: grad norm, finalize, moments, exchange trust, apply
+            "gpu_launches": (5 if args.split else
+                             2 if fused or info["speculative"] else 3) * args.steps,
             "skipped_steps": skips,
-            "mode": ("speculative" if info["speculative"] else
-                     "fused" if info["fused"] else "three kernels"),
+            "mode": ("split step, group of one" + (", fused" if fused else "") if args.split else
+                     "speculative" if info["speculative"] else
+                     "fused" if fused else "three kernels"),
             "clipped_steps": clipped_steps,
             "clocks": clocks,
             "e2e": e2e,

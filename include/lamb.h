@@ -211,14 +211,16 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
  *       forms the grad norm ||g / S||, the clip factor and the skip decision
  *       from the summed norm_exchange (a non-zero inf/NaN count skips the
  *       step on every rank), then updates m and v, finishes every whole
- *       tensor (its trust ratio; small whole tensors are also applied here)
- *       and writes the {sum w^2, sum r^2} of each shared piece to its slot
- *       of tensor_exchange.  t >= 1 fixes the step number; 0 takes the GPU's
+ *       tensor (its trust ratio; small whole tensors are also applied here,
+ *       and on a shard of at most 8 waves of work items -- lamb_get_info's
+ *       fused -- every whole tensor) and writes the {sum w^2, sum r^2} of
+ *       each shared piece to its slot of tensor_exchange.  t >= 1 fixes the step number; 0 takes the GPU's
  *       counter (see lamb_step_async).          -> sum tensor_exchange over the group
  *   lamb_split_apply(h, &seq)
  *       forms the trust ratio of each shared tensor from its summed slot and
- *       applies the update and the bf16 copy; seq (may be NULL) receives the
- *       step's sequence number for lamb_step_result.
+ *       applies the update and the bf16 copy (to the shared tensors, and to
+ *       the whole ones lamb_split_moments has not applied); seq (may be
+ *       NULL) receives the step's sequence number for lamb_step_result.
  *
  * The calls must come in this order (LAMB_ERR_INVALID otherwise, with nothing
  * enqueued).  In between, the handle refuses (LAMB_ERR_INVALID) every call

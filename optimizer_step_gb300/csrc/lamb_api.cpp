@@ -236,6 +236,8 @@ Hyper make_hyper(const lamb_handle* h, float lr, int64_t seq) {
   hy.slot = h->ring_dev + seq % kResultRing;
   hy.parity = int32_t(seq & 1);
   hy.tag = uint32_t(seq % 0xFFFFFFFEll) + 1u;
+  hy.only_shared = 0;
+  hy.pad = 0;
   return hy;
 }
 
@@ -691,7 +693,9 @@ LAMB_API int lamb_split_moments(lamb_handle* h, float lr, int64_t t, float clip)
   if ((rc = wait_for_snapshot(h)) != LAMB_OK) return rc;
   cudaError_t ce = mark(h, r, 1);
   if (ce != cudaSuccess) return cuda_fail(ce, "event record");
-  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, make_hyper(h, lr, seq), false,
+  // A shard of few waves runs the fused kernel here too: it applies every
+  // tensor this rank holds whole, and lamb_split_apply only the shared ones.
+  rc = launch_moments(h->T, h->grid[1], h->hp.grad_dtype, make_hyper(h, lr, seq), h->fused,
                       h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "moments kernel launch");
   h->split_lr = lr;
@@ -711,7 +715,9 @@ LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq_out) {
   if (ce != cudaSuccess) return cuda_fail(ce, "event record");
   int rc = launch_exchange_trust(h->T, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "trust kernel launch");
-  rc = launch_apply(h->T, h->grid[2], make_hyper(h, h->split_lr, seq), h->stream);
+  Hyper hy = make_hyper(h, h->split_lr, seq);
+  hy.only_shared = h->fused ? 1 : 0;
+  rc = launch_apply(h->T, h->grid[2], hy, h->stream);
   if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
   if ((ce = mark(h, r, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
   if ((ce = cudaEventRecord(h->ring_ev[r], h->stream)) != cudaSuccess)

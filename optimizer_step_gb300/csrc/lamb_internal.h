@@ -156,6 +156,9 @@ struct Hyper {
   ResultRecord* slot;        // device view of this step's result slot
   int32_t parity;            // this step's sequence number & 1: which item counters it uses
   uint32_t tag;              // non-zero, different for consecutive steps: trust-ready flags
+  int32_t only_shared;       // apply pass of a split step after the fused kernel: only the
+                             // tensors shared with other ranks are left to apply
+  int32_t pad;
 };
 
 // Sets the calling thread's message returned by lamb_last_error().

@@ -945,6 +945,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_B) moments_kernel(Dev
       if (wi.tensor < 0) continue;  // packs were finished in their moments item
       const TensorDesc d0 = T.td[wi.tensor];
       if (d0.n_items == 1) continue;  // so were tensors of one item
+      if (d0.xslot >= 0) continue;    // shared: applied after the group's exchange
       if (!wait_ready(&T.ready[wi.tensor], hp.tag, &ready_ok)) {
         if (threadIdx.x == 0) {
           atomicOr(reinterpret_cast<unsigned int*>(&T.sc->error), 1u);
@@ -1269,6 +1270,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_kernel(DevTa
     if (wi.tensor < 0) continue;  // packs were finished by the moments kernel
     const TensorDesc d = T.td[wi.tensor];
     if (d.n_items == 1 && d.xslot < 0) continue;  // so were tensors of one item
+    if (hp.only_shared && d.xslot < 0) continue;  // the fused kernel applied it
     const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
     apply_range(d, wi.begin, wi.count, threadIdx.x, kThreads, e, step);
   }
@@ -1355,6 +1357,7 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_C) apply_tma_kernel(D
     if (wi.tensor < 0) continue;  // packs were finished by the moments kernel
     const TensorDesc d = T.td[wi.tensor];
     if (d.n_items == 1 && d.xslot < 0) continue;  // so were tensors of one item
+    if (hp.only_shared && d.xslot < 0) continue;  // the fused kernel applied it
     const float step = __fmul_rn(hp.lr, T.trust[wi.tensor]);
     const int64_t body = (int64_t(wi.count) >> 3) << 3;  // elements in whole vectors
     const int npieces = int((body + kTmaPiece - 1) / kTmaPiece);

@@ -82,6 +82,9 @@ def test_split_step_matches_the_whole_shard(n_ranks):
     n_slots = 1 + max([k for sl in slots for k in sl] + [-1])
     ranks = [_rank_handle(wl, st, gviews, mine, sl, n_slots, "cuda")
              for mine, sl in zip(pieces, slots)]
+    # Shards this small run the fused moments-and-apply kernel in the split
+    # step too (whole tensors applied in lamb_split_moments).
+    assert all(r[0].info()["fused"] == 1 for r in ranks)
     try:
         t = wl.t0
         for k in (1, 2, 3):
@@ -109,6 +112,41 @@ def test_split_step_matches_the_whole_shard(n_ranks):
                     want = np.array([otrust[i] for i, _, _ in mine])
                     assert_close(tr, want, 1e-5, f"{n_ranks} ranks, step {k} trust")
         assert [int(o[0]) for o in outs] == [0] * n_ranks
+    finally:
+        for opt, _, _, _ in ranks:
+            opt.close()
+
+
+def test_split_step_on_shards_of_many_waves():
+    """Two ranks of about 125 M params each: shards of more than 8 waves of
+    work items, so the split step runs the separate moments and apply kernels.
+    One step with clipping active, against the oracle on the unsplit shard."""
+    sizes = [100_000_000, 90_000_003, 60_000_000, 4097, 300, 17]
+    wl = W.Workload("split-large", "split-large", sizes, [1, 1, 1, 1, 0, 0], [], torch.bfloat16,
+                    t0=7, lr=1e-3, clip=0.05, loss_scale=1.0, warm_state=True,
+                    grad_kind="normal", grad_sigma=1e-3, seed=79)
+    st = W.make_state(wl, "cuda")
+    hs = HostState(st, None)
+    gflat, gviews = W.make_grads(wl, 1, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, 2)
+    n_slots = 1 + max([k for sl in slots for k in sl] + [-1])
+    assert n_slots == 1
+    ranks = [_rank_handle(wl, st, gviews, mine, sl, n_slots, "cuda")
+             for mine, sl in zip(pieces, slots)]
+    assert all(r[0].info()["fused"] == 0 for r in ranks)
+    try:
+        g_host = [W.as_bits(x) for x in gviews]
+        seqs = _split_step(ranks, wl, wl.t0, _host_sum)
+        osk, ogn, otrust = oracle_step(wl, hs, g_host, wl.t0)
+        assert osk == 0 and ogn > wl.clip
+        for (opt, _, _, _), q in zip(ranks, seqs):
+            sk, gn, _ = opt.result(q)
+            assert sk is False
+            assert_close(np.array([gn]), np.array([ogn]), 1e-5, "grad_norm")
+        compare_state(st, hs, 1e-5, "two ranks of many waves")
+        for (opt, _, _, _), mine in zip(ranks, pieces):
+            want = np.array([otrust[i] for i, _, _ in mine])
+            assert_close(opt.trust(), want, 1e-5, "trust")
     finally:
         for opt, _, _, _ in ranks:
             opt.close()
