@@ -519,8 +519,9 @@ def run_ours(args, world, rank, local):
                                                  1e9, 1),
                          "floor_28B_frac_of_peak": round(FLOOR_BYTES_PER_PARAM * N /
                                                          (step_ms / 1e3) / 1e9 / peak, 4)},
-            # split: grad norm, finalize, moments, exchange trust, apply
-            "gpu_launches": (5 if args.split else
+            # split: grad norm, finalize, moments, then exchange trust and apply
+            # unless the fused kernel left nothing (a group of one shares nothing)
+            "gpu_launches": ((3 if fused else 5) if args.split else
                              2 if fused or info["speculative"] else 3) * args.steps,
             "skipped_steps": skips,
             "mode": ("split step, group of one" + (", fused" if fused else "") if args.split else

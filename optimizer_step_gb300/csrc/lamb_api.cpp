@@ -713,12 +713,16 @@ LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq_out) {
   const int r = int(seq % kResultRing);
   cudaError_t ce = mark(h, r, 2);
   if (ce != cudaSuccess) return cuda_fail(ce, "event record");
-  int rc = launch_exchange_trust(h->T, h->stream);
-  if (rc) return cuda_fail(cudaError_t(rc), "trust kernel launch");
-  Hyper hy = make_hyper(h, h->split_lr, seq);
-  hy.only_shared = h->fused ? 1 : 0;
-  rc = launch_apply(h->T, h->grid[2], hy, h->stream);
-  if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+  // After the fused kernel only shared tensors are left to apply; with none,
+  // there is nothing to launch.
+  if (!(h->fused && !h->has_shared)) {
+    int rc = launch_exchange_trust(h->T, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "trust kernel launch");
+    Hyper hy = make_hyper(h, h->split_lr, seq);
+    hy.only_shared = h->fused ? 1 : 0;
+    rc = launch_apply(h->T, h->grid[2], hy, h->stream);
+    if (rc) return cuda_fail(cudaError_t(rc), "apply kernel launch");
+  }
   if ((ce = mark(h, r, 3)) != cudaSuccess) return cuda_fail(ce, "event record");
   if ((ce = cudaEventRecord(h->ring_ev[r], h->stream)) != cudaSuccess)
     return cuda_fail(ce, "event record");
