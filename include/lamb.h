@@ -259,9 +259,10 @@ LAMB_API int lamb_split_apply(lamb_handle* h, int64_t* seq);
  *
  * Errors: LAMB_ERR_INVALID and LAMB_ERR_ALIGN are found before anything is
  * enqueued, and the state is untouched.  LAMB_ERR_CUDA means that a launch, a
- * copy or the wait failed, or that a bounded wait inside the apply kernel
- * gave up (its staged copies from HBM never arrived); the state may then be
- * partly updated and should be restored from a snapshot.
+ * copy or the wait failed, or that a bounded wait on the GPU gave up (the
+ * apply kernel's staged copies from HBM, or a tensor's trust ratio or the
+ * step's scalars published by another CTA, never arrived); the state may
+ * then be partly updated and should be restored from a snapshot.
  */
 LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64_t t, float clip,
                        float loss_scale, lamb_result* out);
@@ -290,8 +291,8 @@ LAMB_API int lamb_step(lamb_handle* h, const void* const* grads, float lr, int64
  * until the next work on the handle's stream that writes them).
  *
  * Errors: LAMB_ERR_INVALID and LAMB_ERR_ALIGN before anything is enqueued;
- * LAMB_ERR_CUDA if a launch fails.  A bounded wait that gives up inside the
- * apply kernel is reported by lamb_step_result for that step.
+ * LAMB_ERR_CUDA if a launch fails.  A bounded wait on the GPU that gives up
+ * (see lamb_step) is reported by lamb_step_result for that step.
  */
 LAMB_API int lamb_step_async(lamb_handle* h, const void* const* grads, float lr, float clip,
                              float loss_scale, int64_t* seq);

@@ -351,8 +351,9 @@ int read_result(lamb_handle* h, int64_t seq, lamb_result* out) {
   out->next_loss_scale = v->scale_next;
   out->t = v->t_used;
   if (v->error)
-    return fail(LAMB_ERR_CUDA, "a bounded wait on the GPU gave up (staged copies did not "
-                               "arrive); the state of this step is undefined");
+    return fail(LAMB_ERR_CUDA, "a bounded wait on the GPU gave up (staged copies or a "
+                               "published result did not arrive); the state of this step "
+                               "is undefined");
   return LAMB_OK;
 }
 
