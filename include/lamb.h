@@ -307,7 +307,7 @@ LAMB_API int lamb_step_async(lamb_handle* h, const void* const* grads, float lr,
  *   out   receives the outcome
  *
  * Returns LAMB_ERR_CUDA, with the state of that step undefined, if a bounded
- * wait inside its apply kernel gave up.
+ * wait on the GPU gave up during it (see lamb_step).
  */
 LAMB_API int lamb_step_result(lamb_handle* h, int64_t seq, int32_t wait, lamb_result* out);
 
