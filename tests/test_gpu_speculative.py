@@ -68,6 +68,47 @@ def test_bit_identical_to_ordinary_steps_without_clipping():
         ob.close()
 
 
+def test_dynamic_loss_scaler_equals_ordinary_steps_bit_for_bit():
+    """fp16 grads under a device-resident loss scaler that starts at 2^24:
+    the first steps overflow and are skipped while the scale backs off, then
+    it grows again after 3 clean steps.  A speculative handle follows an
+    ordinary one step by step: the same skip flags and scale sequence, and
+    the same state bit for bit."""
+    wl = _wl([1 << 18, 70001, 4096, 300, 17], clip=0.0, grad_dtype=torch.float16, t0=1)
+    a, b = W.make_state(wl, "cuda"), W.make_state(wl, "cuda")
+    gflat, gviews = W.grad_buffer(wl, "cuda")
+    oa = Lamb(a.w, a.m, a.v, a.w16, wl.wd_flags, grad_dtype=torch.float16)
+    ob = Lamb(b.w, b.m, b.v, b.w16, wl.wd_flags, grad_dtype=torch.float16)
+    m2, v2 = torch.empty_like(b.m_flat), torch.empty_like(b.v_flat)
+    ob.set_speculative(b.views(m2), b.views(v2))
+    cfg = dict(init_scale=2.0 ** 24, growth_factor=2.0, backoff_factor=0.5, growth_interval=3,
+               min_scale=1.0, max_scale=2.0 ** 24)
+    try:
+        oa.set_loss_scaler(**cfg)
+        ob.set_loss_scaler(**cfg)
+        skips, scales, t = [], [], wl.t0
+        for k in range(1, 15):
+            scale = oa.next_loss_scale
+            assert ob.next_loss_scale == scale
+            scales.append(scale)
+            W.fill_grads(wl, k, gflat, loss_scale=scale)
+            ska, _ = oa.step(wl.lr, t, 0.0, 1.0, grads=gviews)
+            skb, _ = ob.step(wl.lr, t, 0.0, 1.0, grads=gviews)
+            assert ska == skb and oa.next_loss_scale == ob.next_loss_scale
+            skips.append(int(ska))
+            t += 0 if ska else 1
+            torch.cuda.synchronize()
+            mb, vb = ob.state_buffers()
+            assert torch.equal(a.w_flat, b.w_flat) and torch.equal(a.w16_flat, b.w16_flat)
+            for ma, mb_, va, vb_ in zip(a.m, mb, a.v, vb):
+                assert torch.equal(ma, mb_) and torch.equal(va, vb_)
+        assert skips[0] == 1 and 0 in skips and sum(skips) >= 2
+        assert max(scales[skips.index(0):]) > min(scales)  # it grew again
+    finally:
+        oa.close()
+        ob.close()
+
+
 def test_clipped_steps_are_redone_and_match_the_oracle():
     """The clip threshold sits inside the range of the grad norms, so some
     steps are clipped (redone from the untouched set) and some are not; fp16

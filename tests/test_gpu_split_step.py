@@ -181,6 +181,58 @@ def test_split_step_with_a_tensor_over_three_ranks_and_fp16_scale():
             opt.close()
 
 
+def test_split_steps_with_a_dynamic_loss_scaler_follow_an_ordinary_handle():
+    """Two ranks, fp16 grads, each rank's handle with the same device-resident
+    loss scaler starting at 2^24 (the first steps overflow), clipping off.
+    Every rank takes the group's skip decision, so both ranks and an ordinary
+    handle over the whole shard give the same skip flags and scale sequence;
+    tensors no rank shares come out bit for bit equal to the ordinary
+    handle's, and the shared one within 1e-6 (its norms are summed in another
+    order)."""
+    wl = _workload(clip=0.0, grad_dtype=torch.float16)
+    st = W.make_state(wl, "cuda")
+    ref = W.make_state(wl, "cuda")
+    gflat, gviews = W.grad_buffer(wl, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, 2)
+    n_slots = 1 + max([k for sl in slots for k in sl] + [-1])
+    ranks = [_rank_handle(wl, st, gviews, mine, sl, n_slots, "cuda")
+             for mine, sl in zip(pieces, slots)]
+    whole = Lamb(ref.w, ref.m, ref.v, ref.w16, wl.wd_flags, grad_dtype=torch.float16)
+    cfg = dict(init_scale=2.0 ** 24, growth_factor=2.0, backoff_factor=0.5, growth_interval=3,
+               min_scale=1.0, max_scale=2.0 ** 24)
+    shared = {i for mine, sl in zip(pieces, slots) for (i, _, _), k in zip(mine, sl) if k >= 0}
+    try:
+        for opt, _, _, _ in ranks:
+            opt.set_loss_scaler(**cfg)
+        whole.set_loss_scaler(**cfg)
+        skips = []
+        for k in range(1, 11):
+            scale = whole.next_loss_scale
+            W.fill_grads(wl, k, gflat, loss_scale=scale)
+            torch.cuda.synchronize()
+            seqs = _split_step(ranks, wl, wl.t0 + k, _host_sum)
+            sk_w, _ = whole.step(wl.lr, wl.t0 + k, 0.0, 1.0, grads=gviews)
+            for (opt, _, _, _), q in zip(ranks, seqs):
+                sk, _, _ = opt.result(q)
+                assert sk == sk_w and opt.next_loss_scale == whole.next_loss_scale
+            skips.append(int(sk_w))
+            torch.cuda.synchronize()
+            for i in range(len(wl.sizes)):
+                for name in ("w", "m", "v", "w16"):
+                    got, want = getattr(st, name)[i], getattr(ref, name)[i]
+                    if i in shared and name in ("w", "w16"):  # the trust ratio differs
+                        rtol = 1e-6 if name == "w" else 2.0 ** -7  # w16: one bf16 ulp
+                        assert torch.allclose(got.float(), want.float(), rtol=rtol, atol=0), \
+                            (k, i, name)
+                    else:
+                        assert torch.equal(got, want), (k, i, name)
+        assert skips[0] == 1 and 0 in skips and shared
+    finally:
+        for opt, _, _, _ in ranks:
+            opt.close()
+        whole.close()
+
+
 def test_ordinary_steps_are_refused_while_a_tensor_is_shared():
     """A shared tensor's trust ratio needs the group's sums, so lamb_step and
     lamb_step_async refuse such a shard (before enqueueing anything); a shard
