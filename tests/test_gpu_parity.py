@@ -394,6 +394,60 @@ def test_deterministic_across_runs():
     assert np.array_equal(outs[0][3], outs[1][3])
 
 
+def test_concurrent_handles_on_their_own_streams_match_solo_runs():
+    """Three handles on three streams -- a fused shard with clipping, a
+    three-kernel one, and a speculative one -- step 8 times each with their
+    steps interleaved and nothing waiting in between, so that their
+    persistent grids share the GPU.  Every kernel's wait is on work that a
+    running CTA holds, so none depends on its grid being resident at once;
+    and every sum is taken in a fixed order.  So each handle ends bit for bit
+    where it ends when it runs alone."""
+    cases = [(custom([1 << 20, 70001, 300, 5000], seed=41, t0=2, clip=0.05), False),
+             (custom([130 << 20, 4096, 17], seed=42, t0=5, clip=0.0), False),
+             (custom([3 << 20, 12288, 9], seed=43, t0=9, clip=0.0, inject={3: "inf"}), True)]
+
+    def run(concurrent):
+        hs = []
+        for wl, spec in cases:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                st = W.make_state(wl, "cuda")
+                flat, views = W.grad_buffer(wl, "cuda")
+            opt = Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags, stream=stream)
+            opt.set_grads(views)
+            if spec:
+                opt.set_speculative(st.views(torch.empty_like(st.m_flat)),
+                                    st.views(torch.empty_like(st.v_flat)))
+            opt.set_step(wl.t0)
+            hs.append([wl, st, flat, opt, stream, []])
+        torch.cuda.synchronize()
+        order = ([(k, h) for k in range(1, 9) for h in hs] if concurrent
+                 else [(k, h) for h in hs for k in range(1, 9)])
+        for k, (wl, st, flat, opt, stream, seqs) in order:
+            with torch.cuda.stream(stream):
+                W.fill_grads(wl, k, flat)
+            seqs.append(opt.step_async(wl.lr, wl.clip, wl.loss_scale))
+        torch.cuda.synchronize()
+        out = []
+        for wl, st, flat, opt, stream, seqs in hs:
+            results = [opt.result(q) for q in seqs]
+            m, v = opt.state_buffers()
+            out.append((results, st.w_flat.clone(), torch.cat([x.flatten() for x in m]),
+                        torch.cat([x.flatten() for x in v]), st.w16_flat.clone(),
+                        opt.trust().copy(), opt.info()))
+            opt.close()
+        return out
+
+    solo, together = run(False), run(True)
+    assert [o[6]["fused"] for o in solo] == [1, 0, 1] and solo[2][6]["speculative"] == 1
+    for a, b in zip(solo, together):
+        assert a[0] == b[0]  # skip flags, grad norms and step numbers
+        for x, y in zip(a[1:5], b[1:5]):
+            assert torch.equal(x, y)
+        assert np.array_equal(a[5], b[5])
+    assert [r[0] for r in solo[2][0]].count(True) == 1  # the planted inf
+
+
 def test_empty_handle_and_errors():
     with Lamb([], [], [], [], []) as opt:
         assert opt.step(1e-3, 1, grads=[]) == (False, 0.0)
