@@ -221,6 +221,33 @@ class Lamb:
         check(self._lib.lamb_split_apply(self._h, ctypes.byref(seq)))
         return int(seq.value)
 
+    def split_step(self, lr: float, clip: float = 0.0, t: int = 0, grads=None,
+                   loss_scale: float = 1.0, all_reduce=None) -> int:
+        """One whole split step: the three phases with the group's two sums
+        between them; returns the step's sequence number for ``result``.
+
+        ``all_reduce(buf)`` must sum the float64 CUDA tensor ``buf`` over the
+        data-parallel group in place, in order with this handle's stream (it
+        is called with that stream current; ``torch.distributed.all_reduce``
+        on an NCCL group does that).  ``None`` stands for a group of one.
+        Slots of ``tensor_exchange`` that this rank does not hold are zeroed
+        before phase 2, so that they add nothing to the sum."""
+        keep = getattr(self, "_exchange_keep", None)
+        if keep is None:
+            raise ValueError("split steps need a handle made with the exchange buffers")
+        norm_exchange, tensor_exchange = keep
+        self.split_norms(grads, loss_scale)
+        with torch.cuda.device(self.device), torch.cuda.stream(self.stream):
+            if all_reduce is not None:
+                all_reduce(norm_exchange)
+            if tensor_exchange is not None:
+                tensor_exchange.zero_()
+        self.split_moments(lr, clip, t)
+        if all_reduce is not None and tensor_exchange is not None:
+            with torch.cuda.device(self.device), torch.cuda.stream(self.stream):
+                all_reduce(tensor_exchange)
+        return self.split_apply()
+
     def info(self) -> dict:
         """What the handle was built with: n_params, one_pass_params (elements
         whose whole step the moments kernel finishes, at 30 B/param),

@@ -233,6 +233,31 @@ def test_split_steps_with_a_dynamic_loss_scaler_follow_an_ordinary_handle():
         whole.close()
 
 
+def test_split_step_of_a_group_of_one_equals_lamb_step():
+    """The binding's whole split step (Lamb.split_step) on a group of one,
+    with no exchange at all, gives lamb_step's result bit for bit, three
+    steps in a row with clipping active."""
+    wl = _workload(clip=0.02)
+    a, b = W.make_state(wl, "cuda"), W.make_state(wl, "cuda")
+    gflat, gviews = W.grad_buffer(wl, "cuda")
+    whole = [(i, 0, n) for i, n in enumerate(wl.sizes)]
+    opt_s, _, _, g = _rank_handle(wl, a, gviews, whole, [-1] * len(whole), 0, "cuda")
+    opt_o = Lamb(b.w, b.m, b.v, b.w16, wl.wd_flags)
+    try:
+        for k in range(1, 4):
+            W.fill_grads(wl, k, gflat)
+            q = opt_s.split_step(wl.lr, wl.clip, wl.t0 + k, grads=g, loss_scale=1.0)
+            sk, gn = opt_o.step(wl.lr, wl.t0 + k, wl.clip, 1.0, grads=gviews)
+            assert opt_s.result(q)[:2] == (sk, gn)
+            torch.cuda.synchronize()
+            for x, y in ((a.w_flat, b.w_flat), (a.m_flat, b.m_flat), (a.v_flat, b.v_flat),
+                         (a.w16_flat, b.w16_flat)):
+                assert torch.equal(x, y)
+    finally:
+        opt_s.close()
+        opt_o.close()
+
+
 def test_ordinary_steps_are_refused_while_a_tensor_is_shared():
     """A shared tensor's trust ratio needs the group's sums, so lamb_step and
     lamb_step_async refuse such a shard (before enqueueing anything); a shard
@@ -329,11 +354,14 @@ def _rank_main(rank, world, port, result_dir):
 
         t = wl.t0
         skipped = []
+        opt = ranks[0][0]
         for k in (1, 2, 3):
             W.fill_grads(wl, k, gflat)
             torch.cuda.synchronize()
             g_host = [W.as_bits(x) for x in gviews]
-            (q,) = _split_step(ranks, wl, t, gloo_sum)
+            # the binding's whole split step, with the group's sums by gloo
+            q = opt.split_step(wl.lr, wl.clip, t, grads=ranks[0][3], loss_scale=wl.loss_scale,
+                               all_reduce=lambda b: gloo_sum([b]))
             sk, gn, _ = ranks[0][0].result(q)
             osk, ogn, _ = oracle_step(wl, hs, g_host, t)
             assert int(sk) == osk
