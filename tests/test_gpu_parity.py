@@ -527,6 +527,34 @@ def test_async_steps_fp16_twenty_with_injected_overflow():
     assert log["t"][-1] == 18  # t started at 1 and two steps were skipped
 
 
+def test_step_result_without_waiting_and_sequence_bounds():
+    """lamb_step_result with wait = 0 answers 'not ready' while the step is
+    still queued behind other work on the handle's stream (a bounded sleep
+    kernel), then the outcome once it has run; sequence numbers not yet
+    given out, and those older than the last 64 steps, are refused."""
+    wl = custom([1 << 20, 300], t0=2)
+    st = W.make_state(wl, "cuda")
+    _, gv = W.make_grads(wl, 1, "cuda")
+    with Lamb(st.w, st.m, st.v, st.w16, wl.wd_flags) as opt:
+        opt.set_grads(gv)
+        opt.set_step(wl.t0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(opt.stream):
+            torch.cuda._sleep(200_000_000)  # about 0.1 s of GPU time, then it ends
+        q = opt.step_async(wl.lr)
+        assert opt.result(q, wait=False) is None
+        done = opt.result(q)
+        assert done[0] is False and done[2] == wl.t0 and math.isfinite(done[1])
+        assert opt.result(q, wait=False) == done
+        with pytest.raises(LambError, match="no step"):
+            opt.result(q + 1)
+        seqs = [opt.step_async(wl.lr) for _ in range(70)]
+        assert opt.result(seqs[-1])[2] == wl.t0 + 70
+        with pytest.raises(LambError, match="only the last 64"):
+            opt.result(q)
+        assert opt.result(seqs[-64])[2] == wl.t0 + 7
+
+
 def test_async_and_synchronous_steps_mix():
     """lamb_step with an explicit t leaves the GPU counter at t+1 (clean) or
     t (skipped), so asynchronous steps continue from there."""
