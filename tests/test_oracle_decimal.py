@@ -171,3 +171,66 @@ def test_fifty_digit_evaluation_sees_a_dropped_momentum_term():
     w16 = [np.zeros(n, np.uint16) for n in c["sizes"]]
     oracle.lamb_step(wo, mo, vo, w16, g, c["wd_flags"], grad_dtype=gd, t=c["t"], **hp)
     assert not half_ulp_ok(mo[0], m_ex[0])[0]
+
+
+def test_oracle_matches_fifty_digit_evaluation_on_random_cases():
+    """The same 50-digit comparison on random hand-sized cases: 1 to 4
+    tensors of 1 to 8 elements, random weight-decay flags, step numbers,
+    betas, eps, learning rates, loss scales and clip thresholds (active or
+    not), bf16 and fp16 grads, and now and then a zero-weight tensor."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    case = st.fixed_dictionaries({
+        "seed": st.integers(0, 2 ** 31 - 1),
+        "sizes": st.lists(st.integers(1, 8), min_size=1, max_size=4),
+        "fp16": st.booleans(),
+        "t": st.integers(1, 2000),
+        "beta1": st.sampled_from([0.0, 0.5, 0.9, 0.95]),
+        "beta2": st.sampled_from([0.9, 0.98, 0.999, 0.9999]),
+        "eps": st.sampled_from([1e-8, 1e-6, 1e-3]),
+        "wd": st.sampled_from([0.0, 0.01, 0.1]),
+        "lr": st.sampled_from([1e-4, 1e-3, 5e-2]),
+        "S": st.sampled_from([1.0, 4.0, 1000.0, 65536.0]),
+        "clip_frac": st.sampled_from([0.0, 0.3, 0.9, 2.0]),
+        "zero_w": st.booleans(),
+    })
+
+    @hyp.settings(max_examples=60, deadline=None, derandomize=True)
+    @hyp.given(case)
+    def prop(c):
+        rng = np.random.default_rng(c["seed"])
+        sizes = c["sizes"]
+        gd = oracle.GRAD_FP16 if c["fp16"] else oracle.GRAD_BF16
+        wd_flags = [int(x) for x in rng.integers(0, 2, len(sizes))]
+        w = [rng.normal(0, 0.02, n).astype(F32) for n in sizes]
+        if c["zero_w"]:
+            w[0][:] = 0
+        first = c["t"] == 1
+        m = [(np.zeros(n) if first else rng.normal(0, 1e-4, n)).astype(F32) for n in sizes]
+        v = [(np.zeros(n) if first else 1e-8 * rng.chisquare(1, n)).astype(F32) for n in sizes]
+        S = c["S"] if c["fp16"] else (c["S"] if c["S"] <= 4.0 else 1.0)
+        g = [bits_of(rng.normal(0, 1e-2, n) * S, gd) for n in sizes]
+        gvals = [values_of(b, gd) for b in g]
+        G = float(np.sqrt(sum(float(np.sum((x / S) ** 2)) for x in gvals)))
+        hyp.assume(G > 0)
+        clip = c["clip_frac"] * G
+        hyp.assume(clip == 0.0 or abs(float(F32(clip)) / G - 1.0) > 1e-6)
+        hp = {k: float(F32(x)) for k, x in dict(
+            beta1=c["beta1"], beta2=c["beta2"], eps=c["eps"], weight_decay=c["wd"],
+            lr=c["lr"], clip=clip, loss_scale=S).items()}
+        Gd, trust, m_ex, v_ex, w_ex = decimal_step(w, m, v, gvals, wd_flags, t=c["t"], **hp)
+        wo, mo, vo = [a.copy() for a in w], [a.copy() for a in m], [a.copy() for a in v]
+        w16 = [np.zeros(n, np.uint16) for n in sizes]
+        skipped, gn, tr = oracle.lamb_step(wo, mo, vo, w16, g, wd_flags, grad_dtype=gd,
+                                           t=c["t"], want_trust=True, **hp)
+        assert skipped == 0
+        assert abs(gn - float(Gd)) <= 1e-14 * float(Gd)
+        for i in range(len(sizes)):
+            assert abs(tr[i] - float(trust[i])) <= 1e-13 * float(trust[i]), (i, tr[i], trust[i])
+            for got, ex, what in ((mo[i], m_ex[i], "m"), (vo[i], v_ex[i], "v"),
+                                  (wo[i], w_ex[i], "w")):
+                ok, ulps = half_ulp_ok(got, ex)
+                assert ok, (c, i, what, ulps)
+
+    prop()
