@@ -48,6 +48,42 @@ def test_small_shapes_one_and_ten_steps(name, grad_dtype):
     run_parity(wl, 10, check_steps=(1, 10))
 
 
+def _random_workload(seed):
+    """A seeded random small shard: 1 to 12 tensors whose sizes mix tiny,
+    pack-edge, one-chunk and several-chunk lengths; random wd flags and zero-
+    weight tensors; random hyperparameters, step number, clip (active or not),
+    grad type and loss scale; warm or zero moments."""
+    rng = np.random.default_rng(seed)
+    pools = [(1, 40), (4090, 4100), (4101, 40000), (40001, 300000)]
+    sizes = []
+    for _ in range(int(rng.integers(1, 13))):
+        lo, hi = pools[int(rng.integers(0, len(pools)))]
+        sizes.append(int(rng.integers(lo, hi + 1)))
+    n = len(sizes)
+    fp16 = bool(rng.integers(0, 2))
+    return W.Workload(
+        f"random{seed}", "random", sizes, [int(x) for x in rng.integers(0, 2, n)],
+        sorted(set(int(x) for x in rng.integers(0, n, int(rng.integers(0, 2))))),
+        torch.float16 if fp16 else torch.bfloat16, t0=int(rng.integers(1, 3000)),
+        lr=float(rng.choice([1e-4, 1e-3, 1e-2])),
+        clip=float(rng.choice([0.0, 1e-3, 0.05, 1e3])),
+        loss_scale=float(rng.choice([256.0, 4096.0, 65536.0])) if fp16 else 1.0,
+        warm_state=bool(rng.integers(0, 2)), grad_kind="normal",
+        grad_sigma=float(rng.choice([1e-4, 1e-3, 1e-2])), seed=1000 + seed,
+        beta1=float(rng.choice([0.0, 0.8, 0.9, 0.95])),
+        beta2=float(rng.choice([0.95, 0.99, 0.999, 0.9999])),
+        eps=float(rng.choice([1e-8, 1e-6, 1e-4])),
+        weight_decay=float(rng.choice([0.0, 0.01, 0.1])))
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_small_shards_match_the_oracle(seed):
+    """Thirty-two seeded random shards (mixed sizes, flags, hyperparameters, grad
+    types, clipping, loss scales), three steps each against the oracle."""
+    wl = _random_workload(seed)
+    run_parity(wl, 3, check_steps=(1, 3))
+
+
 def test_first_step_from_zero_state_with_zero_weight_tensors():
     wl = custom([1000, 50000, 3, 8, 70000], zero=[1, 2], warm=False, t0=1)
     run_parity(wl, 1, check_steps=(1,))
