@@ -117,6 +117,48 @@ def test_split_step_matches_the_whole_shard(n_ranks):
             opt.close()
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shards_cut_over_random_groups(seed):
+    """Seeded random tensor lists cut over 2 to 6 ranks (shared tensors
+    wherever the cuts fall; fp16 or bf16 grads; clipping active or not), two
+    split steps each, against the oracle stepping the unsplit shard."""
+    rng = np.random.default_rng(500 + seed)
+    sizes = [int(rng.choice([rng.integers(1, 50), rng.integers(4090, 4110),
+                             rng.integers(5000, 90000), rng.integers(90000, 400000)]))
+             for _ in range(int(rng.integers(2, 12)))]
+    fp16 = bool(rng.integers(0, 2))
+    wl = W.Workload(f"split-random{seed}", "split-random", sizes,
+                    [int(x) for x in rng.integers(0, 2, len(sizes))], [],
+                    torch.float16 if fp16 else torch.bfloat16, t0=int(rng.integers(1, 500)),
+                    lr=1e-3, clip=float(rng.choice([0.0, 0.01, 100.0])),
+                    loss_scale=1024.0 if fp16 else 1.0, warm_state=True, grad_kind="normal",
+                    grad_sigma=1e-3, seed=900 + seed)
+    n_ranks = int(rng.integers(2, 7))
+    st = W.make_state(wl, "cuda")
+    hs = HostState(st, None)
+    gflat, gviews = W.grad_buffer(wl, "cuda")
+    pieces, slots = W.zero2_pieces(wl.sizes, n_ranks)
+    n_slots = 1 + max([k for sl in slots for k in sl] + [-1])
+    ranks = [_rank_handle(wl, st, gviews, mine, sl, n_slots, "cuda")
+             for mine, sl in zip(pieces, slots) if mine]
+    try:
+        for k in (1, 2):
+            W.fill_grads(wl, k, gflat)
+            torch.cuda.synchronize()
+            g_host = [W.as_bits(x) for x in gviews]
+            seqs = _split_step(ranks, wl, wl.t0 + k - 1, _host_sum)
+            osk, ogn, otrust = oracle_step(wl, hs, g_host, wl.t0 + k - 1)
+            assert osk == 0
+            for (opt, _, _, _), q in zip(ranks, seqs):
+                sk, gn, _ = opt.result(q)
+                assert sk is False
+                assert_close(np.array([gn]), np.array([ogn]), 1e-5, f"step {k} grad_norm")
+            compare_state(st, hs, rtol_for(k), f"seed {seed}, {n_ranks} ranks, step {k}")
+    finally:
+        for opt, _, _, _ in ranks:
+            opt.close()
+
+
 def test_split_step_on_shards_of_many_waves():
     """Two ranks of about 125 M params each: shards of more than 8 waves of
     work items, so the split step runs the separate moments and apply kernels.
