@@ -109,6 +109,26 @@ def test_dynamic_loss_scaler_equals_ordinary_steps_bit_for_bit():
         ob.close()
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shards_speculative_match_the_oracle(seed):
+    """Seeded random shards in speculative mode (sizes from tiny to several
+    chunks, wd flags, grad type and loss scale, clipping off, active or
+    inactive, so that some steps are redone), three steps against the
+    oracle."""
+    rng = np.random.default_rng(700 + seed)
+    sizes = [int(rng.choice([rng.integers(1, 40), rng.integers(4090, 4110),
+                             rng.integers(5000, 60000), rng.integers(60000, 300000)]))
+             for _ in range(int(rng.integers(1, 10)))]
+    fp16 = bool(rng.integers(0, 2))
+    wl = W.Workload(f"spec-random{seed}", "spec-random", sizes,
+                    [int(x) for x in rng.integers(0, 2, len(sizes))], [],
+                    torch.float16 if fp16 else torch.bfloat16, t0=int(rng.integers(1, 800)),
+                    lr=1e-3, clip=float(rng.choice([0.0, 1e-3, 1e3])),
+                    loss_scale=4096.0 if fp16 else 1.0, warm_state=bool(rng.integers(0, 2)),
+                    grad_kind="normal", grad_sigma=1e-3, seed=800 + seed)
+    run_parity(wl, 3, check_steps=(1, 3), speculative=True)
+
+
 def test_clipped_steps_are_redone_and_match_the_oracle():
     """The clip threshold sits inside the range of the grad norms, so some
     steps are clipped (redone from the untouched set) and some are not; fp16
