@@ -84,6 +84,16 @@ def test_random_small_shards_match_the_oracle(seed):
     run_parity(wl, 3, check_steps=(1, 3))
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_small_shards_with_async_steps_match_the_oracle(seed):
+    """Six more seeded random shards, stepped asynchronously (the step number
+    on the GPU) in two batches of 3 and 4 steps, with an inf or a NaN planted
+    in one step: outcomes, step numbers and state against the oracle."""
+    wl = _random_workload(100 + seed)
+    wl.inject = {int(2 + seed % 4): "inf" if seed % 2 else "nan"}
+    run_parity_async(wl, [3, 4])
+
+
 def test_first_step_from_zero_state_with_zero_weight_tensors():
     wl = custom([1000, 50000, 3, 8, 70000], zero=[1, 2], warm=False, t0=1)
     run_parity(wl, 1, check_steps=(1,))
