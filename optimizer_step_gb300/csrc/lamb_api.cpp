@@ -490,7 +490,11 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
   const size_t o_pack = carve(np * sizeof(int32_t));
   size_t o_slot[kGradSlots];
   for (auto& o : o_slot) o = carve(nt * sizeof(void*));
-  const size_t o_g2 = carve(ni * sizeof(double));
+  // item_g2 holds one partial per CTA of the grad-norm kernel (whose grid can
+  // exceed the item count: it cuts items into sub-items) and one per item in
+  // speculative mode.
+  const int64_t g2_entries = std::max<int64_t>(ni, int64_t(per_sm[0]) * sms);
+  const size_t o_g2 = carve(size_t(g2_entries) * sizeof(double));
   const size_t o_wr = carve(ni * sizeof(double2));
   const size_t o_ticket = carve(nt * sizeof(uint32_t));
   const size_t o_trust = carve(nt * sizeof(float));
@@ -578,6 +582,11 @@ LAMB_API int lamb_create_sharded(lamb_handle** out, int32_t n_tensors, const int
     h->split_a = int32_t(split);
     h->grid[0] = int(std::max<int64_t>(
         1, std::min<int64_t>(full, int64_t(ni - n_chunk_items) + n_chunk_items * split)));
+  }
+  if (int64_t(h->grid[0]) > g2_entries || int64_t(h->grid[1]) > g2_entries) {
+    release(h);
+    delete h;
+    return fail(LAMB_ERR_INVALID, "internal: a grid exceeds its partial-sum array");
   }
   *out = h;
   return LAMB_OK;

@@ -135,7 +135,8 @@ struct DevTables {
   const int32_t* pack_ids;
   const TensorDesc* td;
   const void* const* grads;  // per-step grad pointers (device array)
-  double* item_g2;           // per CTA of the grad-norm kernel: sum of raw g^2
+  double* item_g2;           // per CTA of the grad-norm kernel (max(items, its full grid)
+                             // entries): sum of raw g^2; per item in speculative mode
   double2* item_wr;          // per chunk item: (sum w^2, sum r^2)
   uint32_t* tensor_ticket;   // per tensor: chunk items finished this step
   float* trust;              // per tensor: trust ratio of the last step that was not skipped
