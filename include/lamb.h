@@ -31,7 +31,8 @@
  * and owned by the caller (for example as torch tensors) and must stay valid
  * for the life of the handle (state) or until lamb_step returns (grads).  The
  * handle owns only its work table and a small device scratch area (one fp64
- * and one fp64 pair per work item, two words per tensor, a few scalars) plus
+ * per work item or per CTA of one kernel's grid, whichever is more, one fp64
+ * pair per work item, a few words per tensor, a few scalars) plus
  * a small pinned host area; lamb_destroy frees them.
  *
  * Threads and streams.  A handle is bound to the device that was current at
