@@ -58,8 +58,9 @@ def bits16(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16).copy()
 
 
+@pytest.mark.parametrize("speculative", [False, True])
 @pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float16])
-def test_no_kernel_touches_the_guard_bands(grad_dtype):
+def test_no_kernel_touches_the_guard_bands(grad_dtype, speculative):
     dev = torch.device("cuda")
     rng = np.random.default_rng(29)
     n_t = len(SIZES)
@@ -88,6 +89,13 @@ def test_no_kernel_touches_the_guard_bands(grad_dtype):
     opt = Lamb([x.view for x in gw], [x.view for x in gm], [x.view for x in gv],
                [x.view for x in g16], wd, grad_dtype=grad_dtype)
     opt.set_grads([x.view for x in gg])
+    if speculative:  # the second m and v set between guard bands too (its contents: any)
+        gm2 = [Guarded(n, torch.float32, NAN32, dev) for n in SIZES]
+        gv2 = [Guarded(n, torch.float32, NAN32, dev) for n in SIZES]
+        for x in gm2 + gv2:
+            x.view.zero_()
+        everything += gm2 + gv2
+        opt.set_speculative([x.view for x in gm2], [x.view for x in gv2])
     hp = dict(beta1=f32(0.9), beta2=f32(0.999), eps=f32(1e-6), weight_decay=f32(0.01),
               lr=f32(1e-3), clip=f32(0.05), loss_scale=S)
     try:
@@ -104,11 +112,12 @@ def test_no_kernel_touches_the_guard_bands(grad_dtype):
             assert not sk and not osk, "a step saw a non-finite grad: a guard band was read"
             assert_close(np.array([gn]), np.array([ogn]), rtol_for(k), f"step {k} grad_norm")
             rtol = rtol_for(k)
+            cur_m, cur_v = opt.state_buffers()  # speculative mode: the set holding the state
             for i in range(n_t):
                 w_gpu = gw[i].view.cpu().numpy()
                 assert_close(w_gpu, hw[i], rtol, f"step {k} w[{i}] (n={SIZES[i]})")
-                assert_close(gm[i].view.cpu().numpy(), hm[i], rtol, f"step {k} m[{i}]")
-                assert_close(gv[i].view.cpu().numpy(), hv[i], rtol, f"step {k} v[{i}]")
+                assert_close(cur_m[i].cpu().numpy(), hm[i], rtol, f"step {k} m[{i}]")
+                assert_close(cur_v[i].cpu().numpy(), hv[i], rtol, f"step {k} v[{i}]")
                 check_bf16_copy(bits16(g16[i].view), w_gpu, h16[i], hw[i], rtol,
                                 f"step {k} w16[{i}]")
             assert_close(opt.trust(), otr, 1e-5, f"step {k} trust")
