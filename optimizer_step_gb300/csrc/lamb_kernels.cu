@@ -673,6 +673,9 @@ __global__ void __launch_bounds__(kThreads, LAMB_MINBLOCKS_A) grad_norm_kernel(D
 // Split step: the group's summed {sum of raw g^2, inf/NaN count} -> the
 // step's scalars, exactly as the grad-norm kernel's last CTA forms them.
 __global__ void finalize_kernel(DevTables T, NormArgs na, ScaleArgs sa) {
+  // A programmatic dependent of the kernel before it (the grad-norm kernel,
+  // or the collective that summed the partials): wait for its writes.
+  pdl_wait();
   // one warp (publish_step's lanes)
   publish_step(T, na, sa, T.xn[0], !(T.xn[1] == 0.0), int(threadIdx.x & 31));
 }
@@ -1516,11 +1519,6 @@ __global__ void set_step_kernel(StepScalars* sc, int64_t t, double p1, double p2
   sc->p2_next = p2;
 }
 
-int launch_finalize(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, void* stream) {
-  finalize_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(T, na, sa);
-  return int(cudaGetLastError());
-}
-
 int launch_exchange_trust(const DevTables& T, void* stream) {
   const int blocks = T.n_tensors > 0 ? (T.n_tensors + kThreads - 1) / kThreads : 1;
   exchange_trust_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(T);
@@ -1538,9 +1536,9 @@ namespace {
 struct DependentLaunch {
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
-  DependentLaunch(int grid, size_t smem, void* stream) {
+  DependentLaunch(int grid, size_t smem, void* stream, int block = kThreads) {
     cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(unsigned(block));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1550,6 +1548,12 @@ struct DependentLaunch {
   }
 };
 }  // namespace
+
+int launch_finalize(const DevTables& T, const NormArgs& na, const ScaleArgs& sa, void* stream) {
+  DependentLaunch L(1, 0, stream, 32);  // one warp
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, finalize_kernel, T, na, sa);
+  return e != cudaSuccess ? int(e) : int(cudaGetLastError());
+}
 
 int launch_moments(const DevTables& T, int grid, int grad_dtype, const Hyper& hp, bool fused,
                    void* stream) {
