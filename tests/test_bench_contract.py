@@ -79,3 +79,37 @@ def test_cuda_arm_refuses_to_run_without_a_device():
     assert r.returncode != 0
     assert "CUDA device" in (r.stderr + r.stdout)
     assert not _json_lines(r.stdout)
+
+
+def test_algorithmic_byte_accounting():
+    """42 B/param for the three passes (2 + 22 + 18), 30 for tensors finished
+    in one pass (2 + 28 + 0); speculative mode 40 for a step that stands and
+    22 + 40 (28 for one-pass tensors) for one that is clipped and redone."""
+    n, p = 1_000_000, 12_345
+    assert sum(bench.kernel_bytes(n, 0).values()) == 42 * n
+    assert sum(bench.kernel_bytes(n, n).values()) == 30 * n
+    kb = bench.kernel_bytes(n, p)
+    assert kb == {"grad_norm": 2 * n, "moments": 22 * (n - p) + 28 * p, "apply": 18 * (n - p)}
+    assert sum(bench.spec_kernel_bytes(n, p, False).values()) == 40 * n
+    assert bench.spec_kernel_bytes(n, p, True) == {"spec_step": 22 * n,
+                                                   "redo": 40 * (n - p) + 28 * p}
+    assert bench.FLOOR_BYTES_PER_PARAM == 28
+
+
+def test_recorded_traffic_applies_only_to_the_source_it_was_taken_on(tmp_path, monkeypatch):
+    """The committed DRAM-byte record scales with the params while the kernel
+    code is unchanged (comments and blank lines do not count), and is dropped
+    as soon as the code changes."""
+    rec = json.load(open(bench.TRAFFIC_FILE))
+    per = rec["dram_bytes_per_param"]["moments"]
+    src = open(bench.KERNEL_SOURCE).read()
+    assert bench.kernel_source_hash() == rec["kernel_source_sha256"]
+    assert bench.traffic_per_launch("moments", 1000) == pytest.approx(per * 1000)
+    commented = tmp_path / "commented.cu"
+    commented.write_text("// a new comment\n\n" + src.replace("\n", "  // note\n", 3))
+    monkeypatch.setattr(bench, "KERNEL_SOURCE", str(commented))
+    assert bench.traffic_per_launch("moments", 1000) == pytest.approx(per * 1000)
+    changed = tmp_path / "changed.cu"
+    changed.write_text(src + "\nint one_more_line;\n")
+    monkeypatch.setattr(bench, "KERNEL_SOURCE", str(changed))
+    assert bench.traffic_per_launch("moments", 1000) is None
