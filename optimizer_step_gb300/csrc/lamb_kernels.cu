@@ -2,8 +2,8 @@
 //
 // LAMB (You et al., ICLR 2020) as adopted by MegaScale ("MegaScale: Scaling
 // Large Language Model Training to More Than 10,000 GPUs", guided-reading
-// digest, section 2: per-layer learning-rate adaptation), on one rank's ZeRO-2
-// shard (digest section 3).  The step is purely memory-bound (about 25 flops,
+// digest, section 2: a step size scaled layer by layer through a trust ratio),
+// on one rank's ZeRO-2 shard (digest section 3).  The step is purely memory-bound (about 25 flops,
 // one sqrt and one divide per element against 42 bytes), so there is no
 // tensor-core work here: what matters is coalesced 128-bit traffic, enough
 // bytes in flight per SM, and no extra passes over HBM.
@@ -26,7 +26,11 @@
 // items from the same counter and wait, bounded, for their tensor's trust
 // ratio.  In the opt-in speculative mode (a second m/v buffer set) one kernel
 // (spec_step_kernel) does A and B in one read of the inputs and then C, and a
-// redo kernel repeats B and C for a step that turns out clipped.
+// redo kernel repeats B and C for a step that turns out clipped.  In a split
+// step (a ZeRO-2 group whose shards cut tensors) A only writes this shard's
+// partials for the group to sum, finalize_kernel publishes the step from the
+// sums, B writes each shared tensor's sum w^2 and sum r^2 for the group to
+// sum, and exchange_trust_kernel turns those into trust ratios before C.
 // Small tensors (packs) are finished inside B by the warp that owns them, and
 // tensors of a single work item (at most one chunk) by the CTA that owns it,
 // so they cost 30 B/elem instead of 42: the second pass over them hits cache.
