@@ -5,8 +5,8 @@
 // with the CUDA library.  The interface and the method are described in
 // lamb_oracle.h; every step below follows the order given there:
 //   LAMB (You et al., ICLR 2020, the layer-wise trust-ratio form of Adam) as
-//   adopted by MegaScale (guided-reading digest, section 2: per-layer
-//   learning-rate adaptation for 4x larger batches), applied to one rank's
+//   adopted by MegaScale (guided-reading digest, section 2: each layer's step
+//   scaled by its own trust ratio, allowing 4x larger batches), applied to one rank's
 //   ZeRO-2 shard (digest section 3, "Data parallelism (ZeRO-2 style)").
 //
 // Threads only split element ranges; every sum is formed per fixed block and
