@@ -393,9 +393,9 @@ LAMB_API int lamb_set_loss_scaler(lamb_handle* h, const lamb_loss_scaler* cfg);
 
 /*
  * Snapshot of the optimizer state into host memory: the first stage of
- * MegaScale's two-stage checkpoint (guided-reading digest, section 6: copy
- * each GPU's state to pinned host memory in seconds, then write it to
- * storage in the background).
+ * MegaScale's two-stage checkpoint (guided-reading digest, section 6: a quick
+ * device-to-host copy that pauses training only briefly, followed by a
+ * background write from host memory to storage).
  *
  *   host_w, host_m, host_v  host arrays of n_tensors host pointers that
  *                receive each tensor's fp32 w, m and v (size n_i floats;
