@@ -36,6 +36,63 @@ def test_library_exports_every_declared_symbol():
     assert not [s for s in exported if s.startswith("lamb") and s not in declared_symbols()]
 
 
+C_CLIENT = r'''
+/* A plain C99 client of the library: every entry point of the header is
+   referenced, so the link fails if one is missing.  Only lamb_plan and
+   lamb_plan_limits, which need no GPU, are called. */
+#include <stdio.h>
+#include "lamb.h"
+
+typedef void (*entry_point)(void);
+static const entry_point entry_points[] = {
+  (entry_point)lamb_create, (entry_point)lamb_create_sharded, (entry_point)lamb_step,
+  (entry_point)lamb_step_async, (entry_point)lamb_step_result,
+  (entry_point)lamb_split_norms, (entry_point)lamb_split_moments,
+  (entry_point)lamb_split_apply, (entry_point)lamb_get_info,
+  (entry_point)lamb_set_speculative, (entry_point)lamb_state_buffers,
+  (entry_point)lamb_set_step, (entry_point)lamb_loss_scale_device,
+  (entry_point)lamb_set_loss_scaler, (entry_point)lamb_snapshot_async,
+  (entry_point)lamb_snapshot_wait, (entry_point)lamb_destroy, (entry_point)lamb_last_error,
+  (entry_point)lamb_get_trust, (entry_point)lamb_set_timing,
+  (entry_point)lamb_step_kernel_times, (entry_point)lamb_kernel_times,
+  (entry_point)lamb_plan, (entry_point)lamb_plan_limits,
+  (entry_point)lamb_grad_norm_noalloc,
+};
+
+int main(void) {
+  int64_t sizes[3] = {10, 70000, 0}, n_items = 0, n_packs = 0, chunk = 0;
+  lamb_work_item items[8];
+  int32_t packs[4];
+  lamb_plan_limits(&chunk, NULL, NULL, NULL);
+  if (lamb_plan(3, sizes, 0, items, 8, packs, 4, &n_items, &n_packs) != LAMB_OK) {
+    fprintf(stderr, "%s\n", lamb_last_error());
+    return 1;
+  }
+  printf("%d %lld %lld %lld\n", (int)(sizeof entry_points / sizeof entry_points[0]),
+         (long long)chunk, (long long)n_items, (long long)n_packs);
+  return 0;
+}
+'''
+
+
+def test_header_is_plain_c_and_a_c_program_links_and_runs(tmp_path):
+    """The boundary is a C ABI: a C99 program that includes lamb.h and
+    references every entry point compiles with gcc -std=c99 -Wall -Werror,
+    links against the library and runs the host-only calls."""
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    lib = og.library_path()
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.dirname(HEADER), str(src), "-o", str(exe), lib,
+                    "-Wl,-rpath," + os.path.dirname(lib)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == len(declared_symbols())
+    assert int(out[1]) == og.plan_limits()["chunk_elems"]
+    items, packs = og.plan([10, 70000, 0])
+    assert (int(out[2]), int(out[3])) == (len(items), len(packs))
+
+
 def check_plan(sizes, chunk=0):
     lim = og.plan_limits()
     chunk_elems = chunk or lim["chunk_elems"]
